@@ -1,0 +1,116 @@
+"""ORACLE -- plain fp64 CPU attention forward.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package.  It shares no code with the CUDA library
+(``exact_attention_forward_fa2_gb300``) and never imports it; the product path
+never calls it.
+
+``fa2_oracle.c`` holds the arithmetic (see its header for the definition and the
+passages it follows); this file only compiles it with gcc and marshals numpy
+arrays through ctypes.  Pins that tie the oracle to the pages and to mathematics
+live in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa2_oracle.c")
+_LIB = os.path.join(_HERE, "libfa2_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DTYPE_CODE = {np.dtype(np.uint16): 0, np.dtype(np.float32): 1, np.dtype(np.float64): 2}
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle (gcc -O2, OpenMP, no FMA contraction)."""
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp",
+                               "-ffp-contract=off", "-o", tmp, src, "-lm"])
+        os.replace(tmp, out)
+    return out
+
+
+def load(path: str | None = None):
+    """Load the oracle library (building it if needed)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    vp, i32, dbl, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_int64
+    lib.oracle_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dbl, i32, i32]
+    lib.oracle_attn_fwd.restype = i32
+    lib.oracle_attn_fwd_rows.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32,
+                                         dbl, i32, i32]
+    lib.oracle_attn_fwd_rows.restype = i32
+    lib.oracle_attn_fwd_tiled.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dbl, i32,
+                                          i32, i32, i32]
+    lib.oracle_attn_fwd_tiled.restype = i32
+    return lib
+
+
+def _prep(q, k, v):
+    q, k, v = (np.ascontiguousarray(t) for t in (q, k, v))
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE_CODE:
+        raise TypeError("q, k, v must share one dtype: uint16 (bf16 bits), float32 or float64")
+    if q.ndim != 4 or k.ndim != 4 or v.shape != k.shape or q.shape[:2] != k.shape[:2] \
+            or q.shape[3] != k.shape[3]:
+        raise ValueError("expected q [B,H,M,D] and k, v [B,H,N,D]")
+    B, H, M, D = q.shape
+    N = k.shape[2]
+    return q, k, v, B, H, M, N, D, _DTYPE_CODE[q.dtype]
+
+
+def attn_fwd(q, k, v, scale: float, causal: bool, lib=None):
+    """Every row: returns (O [B,H,M,D] fp64, L [B,H,M] fp64)."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v)
+    o = np.empty((B, H, M, D), np.float64)
+    lse = np.empty((B, H, M), np.float64)
+    rc = lib.oracle_attn_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data,
+                             lse.ctypes.data, B, H, M, N, D, float(scale), int(causal), code)
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd failed: {rc}")
+    return o, lse
+
+
+def attn_fwd_rows(q, k, v, scale: float, causal: bool, rows, lib=None):
+    """Selected rows (flat index (b*H+h)*M+i): returns (O [n,D], L [n]) fp64."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    o = np.empty((rows.size, D), np.float64)
+    lse = np.empty((rows.size,), np.float64)
+    rc = lib.oracle_attn_fwd_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, rows.ctypes.data,
+                                  rows.size, o.ctypes.data, lse.ctypes.data, B, H, M, N, D,
+                                  float(scale), int(causal), code)
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_rows failed: {rc}")
+    return o, lse
+
+
+def attn_fwd_tiled(q, k, v, scale: float, causal: bool, block_m: int, block_n: int, lib=None):
+    """The fp64 tiled online-softmax recurrence: returns (O, L) like attn_fwd."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v)
+    o = np.empty((B, H, M, D), np.float64)
+    lse = np.empty((B, H, M), np.float64)
+    rc = lib.oracle_attn_fwd_tiled(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data,
+                                   lse.ctypes.data, B, H, M, N, D, float(scale), int(causal),
+                                   code, int(block_m), int(block_n))
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_tiled failed: {rc}")
+    return o, lse

@@ -1,0 +1,251 @@
+/*
+ * ORACLE -- plain fp64 CPU attention forward.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the package's smoke check and the bench's CPU-baseline leg may
+ * load this file's library.  It shares no code, header, table or helper with the
+ * CUDA library, and the product path never calls it.
+ *
+ * What it computes (the plain definition the FlashAttention-2 forward reaches
+ * exactly, up to rounding order):
+ *   for every batch b, head h and query row i,
+ *     s_j  = scale * sum_d q[i,d] k[j,d]      for every visible key j
+ *     m    = max_j s_j,   w_j = exp(s_j - m),   l = sum_j w_j
+ *     O[i] = sum_j w_j v[j] / l,                L[i] = m + ln l
+ *   Visible: j < N, and j <= i when causal (top-left aligned).
+ * Sources: "From FlashAttention to FlashAttention 2", Background: FlashAttention 1
+ * (standard attention softmax(QK^T/sqrt d)V and the stored logsumexp
+ * L = m + log l); "FlashAttention-2 from PyTorch to Triton", introduction
+ * (L_i = m_i + log l_i = log sum_k exp S_ik) and its test file's reference
+ * (masked scores, logsumexp over the last axis); "Writing FlashAttention 2 in
+ * Triton", Step 4 (causal: query row m sees key n iff m >= n).
+ *
+ * A second entry point, oracle_attn_fwd_tiled, runs the pages' tiled online
+ * softmax recurrence in fp64 (query tiles outer, key tiles inner, running m, l
+ * and unnormalised O rescaled by exp(m_old - m_new), one divide at the end;
+ * "FlashAttention-2 from PyTorch to Triton", the PyTorch FlashAttentionPytorch
+ * forward and the Triton kernel's inner loop).  It exists to pin the identity
+ * "tiled recurrence == two-pass softmax" that the GPU path relies on.
+ *
+ * Inputs are the same host arrays the GPU receives: dtype 0 = bf16 bit
+ * patterns, 1 = fp32, 2 = fp64 (oracle-only, for closed-form pins).  Every
+ * element is widened to fp64 before use, so the oracle measures only the
+ * kernel's arithmetic error.  Layouts: q [B,H,M,D], k and v [B,H,N,D],
+ * o [B,H,M,D] fp64, lse [B,H,M] fp64, all contiguous.
+ *
+ * Return value: 0 on success, -1 on invalid sizes, -2 on allocation failure,
+ * -3 if a row had no visible key (cannot happen for N >= 1).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double widen(const void* base, int64_t idx, int dtype) {
+  if (dtype == 0) {
+    uint32_t u = (uint32_t)((const uint16_t*)base)[idx] << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+  }
+  if (dtype == 1) return (double)((const float*)base)[idx];
+  return ((const double*)base)[idx];
+}
+
+static int check_sizes(int B, int H, int M, int N, int D, int dtype) {
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || D <= 0) return -1;
+  if (dtype < 0 || dtype > 2) return -1;
+  return 0;
+}
+
+/* Number of keys visible to query row i. */
+static int64_t visible_keys(int64_t i, int N, int causal) {
+  if (!causal) return N;
+  return (i + 1 < N) ? i + 1 : N;
+}
+
+/* One query row of one (b,h): the definition, with all scores of the row formed
+ * explicitly.  w must hold N doubles. */
+static int attn_row(const void* q, const void* k, const void* v, int dtype,
+                    int64_t bh, int64_t i, int M, int N, int D, double scale,
+                    int causal, double* o_row, double* lse, double* w) {
+  const int64_t qoff = (bh * M + i) * (int64_t)D;
+  const int64_t kvoff = bh * (int64_t)N * D;
+  const int64_t nvis = visible_keys(i, N, causal);
+  if (nvis <= 0) return -3;
+
+  double m = -INFINITY;
+  for (int64_t j = 0; j < nvis; ++j) {
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d)
+      dot += widen(q, qoff + d, dtype) * widen(k, kvoff + j * D + d, dtype);
+    w[j] = scale * dot;
+    if (w[j] > m) m = w[j];
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j < nvis; ++j) {
+    w[j] = exp(w[j] - m);
+    l += w[j];
+  }
+  for (int d = 0; d < D; ++d) {
+    double acc = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) acc += w[j] * widen(v, kvoff + j * D + d, dtype);
+    o_row[d] = acc / l;
+  }
+  *lse = m + log(l);
+  return 0;
+}
+
+/* Every row of every (b,h). */
+int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, double* lse,
+                    int B, int H, int M, int N, int D, double scale, int causal,
+                    int dtype) {
+  if (check_sizes(B, H, M, N, D, dtype)) return -1;
+  const int64_t rows = (int64_t)B * H * M;
+  int status = 0;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!w) {
+#pragma omp atomic write
+      status = -2;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t r = 0; r < rows; ++r) {
+        int64_t bh = r / M, i = r % M;
+        int rc = attn_row(q, k, v, dtype, bh, i, M, N, D, scale, causal, o + r * D, lse + r, w);
+        if (rc) {
+#pragma omp atomic write
+          status = rc;
+        }
+      }
+      free(w);
+    }
+  }
+  return status;
+}
+
+/* Only the listed rows; rows[t] is the flat row index (b*H + h)*M + i.
+ * o is [nrows, D], lse is [nrows]. */
+int oracle_attn_fwd_rows(const void* q, const void* k, const void* v,
+                         const int64_t* rows, int64_t nrows, double* o, double* lse,
+                         int B, int H, int M, int N, int D, double scale, int causal,
+                         int dtype) {
+  if (check_sizes(B, H, M, N, D, dtype)) return -1;
+  const int64_t total = (int64_t)B * H * M;
+  for (int64_t t = 0; t < nrows; ++t)
+    if (rows[t] < 0 || rows[t] >= total) return -1;
+  int status = 0;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!w) {
+#pragma omp atomic write
+      status = -2;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int64_t t = 0; t < nrows; ++t) {
+        int64_t r = rows[t];
+        int rc = attn_row(q, k, v, dtype, r / M, r % M, M, N, D, scale, causal,
+                          o + t * D, lse + t, w);
+        if (rc) {
+#pragma omp atomic write
+          status = rc;
+        }
+      }
+      free(w);
+    }
+  }
+  return status;
+}
+
+/* The tiled online-softmax recurrence in fp64, query tiles of BM rows outer,
+ * key tiles of BN rows inner.  Per query row the state is (m, l, O~):
+ *   m_new = max(m, max_j s_j);  alpha = exp(m - m_new);  p_j = exp(s_j - m_new)
+ *   l = alpha l + sum_j p_j;    O~ = alpha O~ + sum_j p_j v_j;   m = m_new
+ * with masked keys (j >= N, or j > i when causal) excluded, and at the end
+ * O = O~ / l, L = m + ln l.  With m = -inf before the first key the factor
+ * alpha = exp(-inf) is 0, so the first tile needs no special case. */
+int oracle_attn_fwd_tiled(const void* q, const void* k, const void* v, double* o, double* lse,
+                          int B, int H, int M, int N, int D, double scale, int causal,
+                          int dtype, int BM, int BN) {
+  if (check_sizes(B, H, M, N, D, dtype) || BM <= 0 || BN <= 0) return -1;
+  const int64_t n_qtiles = (M + BM - 1) / BM;
+  const int64_t units = (int64_t)B * H * n_qtiles;
+  int status = 0;
+#pragma omp parallel
+  {
+    double* m_run = (double*)malloc(sizeof(double) * (size_t)BM);
+    double* l_run = (double*)malloc(sizeof(double) * (size_t)BM);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)BM * D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)BM * BN);
+    if (!m_run || !l_run || !acc || !s) {
+#pragma omp atomic write
+      status = -2;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t u = 0; u < units; ++u) {
+        const int64_t bh = u / n_qtiles, qt = u % n_qtiles;
+        const int64_t i0 = qt * BM;
+        const int rows = (int)((i0 + BM <= M) ? BM : (M - i0));
+        const int64_t kvoff = bh * (int64_t)N * D;
+        for (int r = 0; r < rows; ++r) {
+          m_run[r] = -INFINITY;
+          l_run[r] = 0.0;
+          for (int d = 0; d < D; ++d) acc[(int64_t)r * D + d] = 0.0;
+        }
+        for (int64_t j0 = 0; j0 < N; j0 += BN) {
+          const int cols = (int)((j0 + BN <= N) ? BN : (N - j0));
+          for (int r = 0; r < rows; ++r) {
+            const int64_t i = i0 + r;
+            const int64_t qoff = (bh * M + i) * (int64_t)D;
+            double tile_max = -INFINITY;
+            for (int c = 0; c < cols; ++c) {
+              const int64_t j = j0 + c;
+              if (causal && j > i) {
+                s[(int64_t)r * BN + c] = -INFINITY;
+                continue;
+              }
+              double dot = 0.0;
+              for (int d = 0; d < D; ++d)
+                dot += widen(q, qoff + d, dtype) * widen(k, kvoff + j * D + d, dtype);
+              s[(int64_t)r * BN + c] = scale * dot;
+              if (s[(int64_t)r * BN + c] > tile_max) tile_max = s[(int64_t)r * BN + c];
+            }
+            const double m_new = (tile_max > m_run[r]) ? tile_max : m_run[r];
+            if (m_new == -INFINITY) continue; /* no visible key yet: state unchanged */
+            const double alpha = exp(m_run[r] - m_new);
+            double rowsum = 0.0;
+            for (int c = 0; c < cols; ++c) {
+              double p = exp(s[(int64_t)r * BN + c] - m_new);
+              s[(int64_t)r * BN + c] = p;
+              rowsum += p;
+            }
+            l_run[r] = alpha * l_run[r] + rowsum;
+            for (int d = 0; d < D; ++d) {
+              double pv = 0.0;
+              for (int c = 0; c < cols; ++c)
+                pv += s[(int64_t)r * BN + c] * widen(v, kvoff + (j0 + c) * D + d, dtype);
+              acc[(int64_t)r * D + d] = alpha * acc[(int64_t)r * D + d] + pv;
+            }
+            m_run[r] = m_new;
+          }
+        }
+        for (int r = 0; r < rows; ++r) {
+          const int64_t row = bh * M + i0 + r;
+          if (l_run[r] <= 0.0) {
+#pragma omp atomic write
+            status = -3;
+            continue;
+          }
+          for (int d = 0; d < D; ++d) o[row * D + d] = acc[(int64_t)r * D + d] / l_run[r];
+          lse[row] = m_run[r] + log(l_run[r]);
+        }
+      }
+    }
+    free(m_run);
+    free(l_run);
+    free(acc);
+    free(s);
+  }
+  return status;
+}

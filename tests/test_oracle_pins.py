@@ -1,0 +1,319 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+- hand-derived worked examples (tests/golden/worked_examples.json);
+- brute force with library routines: the whole score matrix materialised by a
+  numpy matmul, L from scipy's logsumexp, P = exp(S - L) (the backward-pass
+  identity of "FlashAttention-2 from PyTorch to Triton", introduction);
+- PyTorch's CPU scaled_dot_product_attention in fp64 as a third opinion;
+- closed forms and invariants: K = 0 gives the mean of the visible V rows and
+  L = ln(#visible); one key gives O = V_0; O rows are convex combinations of V
+  rows; causal row 0 equals V row 0; key/value permutation invariance; affine
+  equivariance in V; the tiled online recurrence equals the two-pass softmax.
+
+test_planted_mistakes_are_caught then plants plausible mistakes in a copy of the
+oracle's C source (a dropped term, a wrong sign or index, a transposed operand,
+an off-by-one causal bound) and checks that every mutant fails at least one pin.
+"""
+import json
+import math
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import seeded_inputs as si
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")
+
+
+def widen(x):
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return si.bf16_bits_to_f32(x).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def brute_force(q, k, v, scale, causal):
+    """Materialise S, mask, L = logsumexp, P = exp(S - L), O = P V (fp64)."""
+    q, k, v = widen(q), widen(k), widen(v)
+    M, N = q.shape[2], k.shape[2]
+    s = scale * np.matmul(q, np.swapaxes(k, -1, -2))
+    if causal:
+        hidden = np.arange(N)[None, :] > np.arange(M)[:, None]
+        s = np.where(hidden, -np.inf, s)
+    lse = scipy.special.logsumexp(s, axis=-1)
+    p = np.exp(s - lse[..., None])
+    return np.matmul(p, v), lse
+
+
+def rand_inputs(seed, B, H, M, N, D, dtype, sigma=1.0):
+    q = si.normal(seed, 1, (B, H, M, D), sigma, dtype)
+    k = si.normal(seed, 2, (B, H, N, D), sigma, dtype)
+    v = si.normal(seed, 3, (B, H, N, D), 1.0, dtype)
+    return q, k, v
+
+
+def max_err(a, b):
+    return float(np.max(np.abs(np.asarray(a) - np.asarray(b))))
+
+
+# ---------------------------------------------------------------- pin suite
+def golden_errors(lib):
+    errs = []
+    with open(GOLDEN) as f:
+        data = json.load(f)
+    tol = data["tolerance"]
+    for c in data["cases"]:
+        q, k, v = (np.array(c[n], np.float64) for n in ("q", "k", "v"))
+        o, lse = oracle.attn_fwd(q, k, v, c["scale"], c["causal"], lib=lib)
+        e = max(max_err(o, c["o"]), max_err(lse, c["lse"]))
+        if not e <= tol:
+            errs.append(f"golden {c['name']}: {e}")
+    return errs
+
+
+BRUTE_SHAPES = [  # (B, H, M, N, D)
+    (1, 1, 1, 1, 1), (1, 1, 1, 7, 2), (1, 1, 7, 1, 2), (2, 1, 3, 3, 64), (1, 2, 16, 16, 2),
+    (1, 1, 37, 53, 64), (1, 1, 53, 37, 2), (2, 2, 7, 16, 1),
+]
+
+
+def brute_errors(lib, dtypes=(si.FP64, si.FP32, si.BF16), shapes=BRUTE_SHAPES):
+    errs = []
+    for si_dtype in dtypes:
+        for n, (B, H, M, N, D) in enumerate(shapes):
+            for causal in (False, True):
+                q, k, v = rand_inputs(100 + n, B, H, M, N, D, si_dtype)
+                scale = 1.0 / math.sqrt(D)
+                o, lse = oracle.attn_fwd(q, k, v, scale, causal, lib=lib)
+                ob, lb = brute_force(q, k, v, scale, causal)
+                e = max(max_err(o, ob), max_err(lse, lb))
+                if not e <= 1e-12:
+                    errs.append(f"brute {si_dtype} {(B, H, M, N, D)} causal={causal}: {e}")
+    return errs
+
+
+def large_score_errors(lib):
+    """Scores of magnitude ~1e3: exp without the max subtraction overflows."""
+    errs = []
+    q, k, v = rand_inputs(7, 1, 1, 9, 11, 4, si.FP64, sigma=30.0)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, 1.0, causal, lib=lib)
+        ob, lb = brute_force(q, k, v, 1.0, causal)
+        e = max(max_err(o, ob), max_err(lse, lb) / max(1.0, float(np.max(np.abs(lb)))))
+        if not e <= 1e-12:
+            errs.append(f"large scores causal={causal}: {e}")
+    return errs
+
+
+def invariant_errors(lib):
+    errs = []
+    B, H, M, N, D = 2, 2, 19, 23, 8
+    q, k, v = rand_inputs(11, B, H, M, N, D, si.FP64)
+    scale = 0.37
+    for causal in (False, True):
+        nvis = np.minimum(np.arange(M) + 1, N) if causal else np.full(M, N)
+        # K == 0: uniform weights over the visible keys
+        o, lse = oracle.attn_fwd(q, np.zeros_like(k), v, scale, causal, lib=lib)
+        cs = np.cumsum(v, axis=2)
+        mean = np.stack([cs[:, :, n - 1, :] / n for n in nvis], axis=2)
+        if max_err(o, mean) > 1e-12 or max_err(lse, np.broadcast_to(np.log(nvis), lse.shape)) > 1e-12:
+            errs.append(f"K=0 causal={causal}")
+        # convex hull of the visible V rows
+        o, lse = oracle.attn_fwd(q, k, v, scale, causal, lib=lib)
+        for i in range(M):
+            vis = v[:, :, : nvis[i], :]
+            lo, hi = vis.min(axis=2), vis.max(axis=2)
+            if np.any(o[:, :, i, :] < lo - 1e-12) or np.any(o[:, :, i, :] > hi + 1e-12):
+                errs.append(f"hull row {i} causal={causal}")
+                break
+        # affine equivariance in V
+        a, c = -1.75, 0.5
+        o2, lse2 = oracle.attn_fwd(q, k, a * v + c, scale, causal, lib=lib)
+        if max_err(o2, a * o + c) > 1e-12 or max_err(lse2, lse) > 0:
+            errs.append(f"affine causal={causal}")
+        # causal row 0 is V row 0 and its L is its own score
+        if causal:
+            if max_err(o[:, :, 0, :], v[:, :, 0, :]) > 1e-12:
+                errs.append("causal row 0 != V row 0")
+            s00 = scale * np.sum(q[:, :, 0, :] * k[:, :, 0, :], axis=-1)
+            if max_err(lse[:, :, 0], s00) > 1e-12:
+                errs.append("causal row 0 L != s_00")
+    # key/value permutation (non-causal only)
+    perm = np.random.default_rng(3).permutation(N)
+    o, lse = oracle.attn_fwd(q, k, v, scale, False, lib=lib)
+    o2, lse2 = oracle.attn_fwd(q, k[:, :, perm], v[:, :, perm], scale, False, lib=lib)
+    if max_err(o, o2) > 1e-12 or max_err(lse, lse2) > 1e-12:
+        errs.append("permutation")
+    # a single key: O = V_0, L = scale q.k_0
+    o, lse = oracle.attn_fwd(q, k[:, :, :1], v[:, :, :1], scale, False, lib=lib)
+    if max_err(o, np.broadcast_to(v[:, :, :1], o.shape)) > 1e-12:
+        errs.append("N=1 O")
+    if max_err(lse, scale * np.einsum("bhmd,bhd->bhm", q, k[:, :, 0])) > 1e-12:
+        errs.append("N=1 L")
+    return errs
+
+
+def rows_errors(lib):
+    errs = []
+    B, H, M, N, D = 2, 3, 21, 17, 16
+    q, k, v = rand_inputs(5, B, H, M, N, D, si.BF16)
+    rows = np.array([0, 5, 20, 21, 62, B * H * M - 1], np.int64)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, 0.25, causal, lib=lib)
+        orow, lrow = oracle.attn_fwd_rows(q, k, v, 0.25, causal, rows, lib=lib)
+        if max_err(orow, o.reshape(-1, D)[rows]) > 0 or max_err(lrow, lse.reshape(-1)[rows]) > 0:
+            errs.append(f"rows causal={causal}")
+    return errs
+
+
+TILINGS = [(1, 1), (16, 16), (7, 5), (128, 128), (64, 37), (3, 64)]
+
+
+def tiled_errors(lib):
+    errs = []
+    for n, (B, H, M, N, D) in enumerate([(1, 2, 70, 70, 8), (2, 1, 33, 100, 4), (1, 1, 100, 33, 16)]):
+        for dtype in (si.FP64, si.BF16):
+            q, k, v = rand_inputs(40 + n, B, H, M, N, D, dtype, sigma=2.0)
+            for causal in (False, True):
+                ob, lb = brute_force(q, k, v, 0.3, causal)
+                for bm, bn in TILINGS:
+                    o, lse = oracle.attn_fwd_tiled(q, k, v, 0.3, causal, bm, bn, lib=lib)
+                    e = max(max_err(o, ob), max_err(lse, lb))
+                    if not e <= 1e-12:
+                        errs.append(f"tiled {bm}x{bn} {(B, H, M, N, D)} causal={causal}: {e}")
+    return errs
+
+
+def all_pin_errors(lib):
+    errs = []
+    for check in (golden_errors, brute_errors, large_score_errors, invariant_errors,
+                  rows_errors, tiled_errors):
+        try:
+            errs += check(lib)
+        except Exception as exc:  # a mutant may also crash or return an error code
+            errs.append(f"{check.__name__} raised {exc!r}")
+    return errs
+
+
+# ---------------------------------------------------------------- tests
+def test_generator_is_counter_based_and_deterministic():
+    a = si.normal(9, 2, (1000,), 1.0, si.FP64)
+    b = si.normal(9, 2, (400,), 1.0, si.FP64, offset=600)
+    assert np.array_equal(a[600:], b)
+    assert np.array_equal(a, si.normal(9, 2, (1000,), 1.0, si.FP64))
+    assert not np.array_equal(a, si.normal(9, 3, (1000,), 1.0, si.FP64))
+    big = si.normal(1, 1, (200000,), 1.0, si.FP64)
+    assert abs(big.mean()) < 0.01 and abs(big.std() - 1.0) < 0.01
+    bits = si.normal(9, 2, (1000,), 1.0, si.BF16)
+    f32 = si.normal(9, 2, (1000,), 1.0, si.FP32)
+    # bf16 = RNE of the fp32 value: within half a bf16 ulp
+    w = si.bf16_bits_to_f32(bits)
+    assert np.all(np.abs(w - f32) <= np.abs(f32) * 2.0 ** -8 + 1e-30)
+    assert np.array_equal(si.f64_to_bf16_bits(f32.astype(np.float64)), bits)
+
+
+def test_golden_worked_examples(oracle_lib):
+    assert golden_errors(oracle_lib) == []
+
+
+def test_matches_brute_force(oracle_lib):
+    assert brute_errors(oracle_lib) == []
+
+
+def test_large_scores_stable(oracle_lib):
+    assert large_score_errors(oracle_lib) == []
+
+
+def test_invariants(oracle_lib):
+    assert invariant_errors(oracle_lib) == []
+
+
+def test_row_sampled_entry_matches_full(oracle_lib):
+    assert rows_errors(oracle_lib) == []
+
+
+def test_tiled_recurrence_equals_two_pass(oracle_lib):
+    assert tiled_errors(oracle_lib) == []
+
+
+def test_matches_torch_sdpa_fp64():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    for n, (B, H, M, N, D) in enumerate([(2, 3, 17, 17, 32), (1, 2, 40, 24, 64), (1, 1, 24, 40, 8)]):
+        q, k, v = rand_inputs(60 + n, B, H, M, N, D, si.FP32)
+        for causal in (False, True):
+            o, lse = oracle.attn_fwd(q, k, v, 1.0 / math.sqrt(D), causal)
+            tq, tk, tv = (torch.from_numpy(widen(t)) for t in (q, k, v))
+            to = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal)
+            s = tq @ tk.transpose(-1, -2) / math.sqrt(D)
+            if causal:
+                s = s.masked_fill(~torch.ones(M, N, dtype=torch.bool).tril(), float("-inf"))
+            tl = torch.logsumexp(s, dim=-1)
+            assert max_err(o, to.numpy()) < 1e-12
+            assert max_err(lse, tl.numpy()) < 1e-12
+
+
+def test_rejects_bad_sizes(oracle_lib):
+    q = np.zeros((1, 1, 4, 8))
+    with pytest.raises(ValueError):
+        oracle.attn_fwd(q, np.zeros((1, 1, 4, 7)), np.zeros((1, 1, 4, 7)), 1.0, False)
+    with pytest.raises(RuntimeError):
+        oracle.attn_fwd(q, np.zeros((1, 1, 0, 8)), np.zeros((1, 1, 0, 8)), 1.0, False)
+
+
+# Each mutant: (name, original snippet, replacement, count). The snippets are
+# taken from fa2_oracle.c; the test fails loudly if one no longer matches.
+MUTANTS = [
+    ("causal excludes the diagonal", "return (i + 1 < N) ? i + 1 : N;", "return (i < N) ? i : N;", 1),
+    ("causal one key too many", "return (i + 1 < N) ? i + 1 : N;", "return (i + 2 < N) ? i + 2 : N;", 1),
+    ("causal ignored", "if (!causal) return N;", "if (1) return N;", 1),
+    ("scale dropped", "w[j] = scale * dot;", "w[j] = dot;", 1),
+    ("K read transposed", "widen(k, kvoff + j * D + d, dtype);\n    w[j]",
+     "widen(k, kvoff + d * N + j, dtype);\n    w[j]", 1),
+    ("exp sign flipped", "w[j] = exp(w[j] - m);", "w[j] = exp(m - w[j]);", 1),
+    ("max not subtracted", "w[j] = exp(w[j] - m);", "w[j] = exp(w[j]);", 1),
+    ("no final divide", "o_row[d] = acc / l;", "o_row[d] = acc;", 1),
+    ("L without log", "*lse = m + log(l);", "*lse = m + l;", 1),
+    ("L in log2", "*lse = m + log(l);", "*lse = m + log2(l);", 1),
+    ("L missing max", "*lse = m + log(l);", "*lse = log(l);", 1),
+    ("V always row 0", "acc += w[j] * widen(v, kvoff + j * D + d, dtype);",
+     "acc += w[j] * widen(v, kvoff + d, dtype);", 1),
+    ("Q row offset dropped", "const int64_t qoff = (bh * M + i) * (int64_t)D;\n  const int64_t kvoff = bh",
+     "const int64_t qoff = (bh * M) * (int64_t)D;\n  const int64_t kvoff = bh", 1),
+    ("K/V head offset dropped", "const int64_t kvoff = bh * (int64_t)N * D;\n  const int64_t nvis",
+     "const int64_t kvoff = 0;\n  const int64_t nvis", 1),
+    ("tiled: O not rescaled", "acc[(int64_t)r * D + d] = alpha * acc[(int64_t)r * D + d] + pv;",
+     "acc[(int64_t)r * D + d] = acc[(int64_t)r * D + d] + pv;", 1),
+    ("tiled: l not rescaled", "l_run[r] = alpha * l_run[r] + rowsum;", "l_run[r] = l_run[r] + rowsum;", 1),
+    ("tiled: alpha sign flipped", "const double alpha = exp(m_run[r] - m_new);",
+     "const double alpha = exp(m_new - m_run[r]);", 1),
+    ("tiled: causal mask off by one", "if (causal && j > i) {", "if (causal && j >= i) {", 1),
+    ("tiled: ragged last key tile dropped", "for (int64_t j0 = 0; j0 < N; j0 += BN) {",
+     "for (int64_t j0 = 0; j0 + BN <= N; j0 += BN) {", 1),
+]
+
+
+def test_planted_mistakes_are_caught():
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(oracle._SRC).read()
+    assert all_pin_errors(oracle.load()) == [], "the unmodified oracle must pass every pin"
+    survived = []
+    with tempfile.TemporaryDirectory() as tmp:
+        for n, (name, old, new, count) in enumerate(MUTANTS):
+            assert src.count(old) == count, f"mutant {name!r}: snippet not found in the oracle source"
+            msrc = os.path.join(tmp, f"m{n}.c")
+            mlib = os.path.join(tmp, f"m{n}.so")
+            with open(msrc, "w") as f:
+                f.write(src.replace(old, new))
+            subprocess.check_call(["gcc", "-O1", "-fPIC", "-shared", "-fopenmp", "-o", mlib, msrc, "-lm"])
+            errs = all_pin_errors(oracle.load(mlib))
+            if not errs:
+                survived.append(name)
+    assert survived == [], f"mutants not caught by any pin: {survived}"
