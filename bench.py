@@ -1,0 +1,389 @@
+"""Bench: FlashAttention-2 forward TFLOP/s on GB300 and its fraction of the
+dense bf16 tensor-core peak.
+
+One step = one fa2_fwd call (the whole forward: every row of the hot path) over
+the workload below, inputs resident in HBM.  Prints ONE JSON line.
+
+Workload: bf16, B=2, H=16, M=N=8192, D=128, causal, scale 1/sqrt(128) (the
+configuration the >= 50%-of-peak target is stated on); FLOP = 4*B*H*M*N*D / 2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores (a bounded sample
+of the same workload per step): the method has no runnable reference
+implementation, so the oracle is the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+WORKLOAD = "bf16_2x16x8192x8192x128_causal"
+METRIC = "FA2 fwd TFLOP/s (4BHMND, 1/2 causal) and % of GB300 dense tensor peak"
+UNIT = "TFLOP/s"
+KERNEL = "fa2_fwd_kernel"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fa2_fwd_kernel_bf16_2x16x8192x8192x128_causal.md")
+L2_FLUSH_BYTES = 256 << 20
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_forward_fa2_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic_per_launch():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (its recorded source hash matches)."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    text = open(PROFILE_SUMMARY).read()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """Samples the GPU's SM clock, power and clock-event (throttle) reasons
+    through NVML every 2 ms on a background thread while the timed region runs
+    (NVML is called through ctypes; nvidia-smi's 200 ms period is longer than
+    the whole timed region)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, log_path: str | None = None):
+        self.index = device_index
+        self.log_path = log_path
+        self.samples = []
+        self.nvml = None
+
+    def _open(self):
+        import ctypes
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return None
+        if nvml.nvmlInit_v2() != 0:
+            return None
+        handle = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(self.index)
+            bus = getattr(props, "pci_bus_id", None)
+            if bus is not None:
+                pci = f"{getattr(props, 'pci_domain_id', 0):08X}:{bus:02X}:{getattr(props, 'pci_device_id', 0):02X}.0"
+                ok = nvml.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(handle)) == 0
+        except Exception:
+            ok = False
+        if not ok and nvml.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(handle)) != 0:
+            return None
+        self.handle = handle
+        self.reason_fn = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint(0)
+        nvml.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        return nvml
+
+    def _run(self):
+        import ctypes
+        mhz, reasons, mw = ctypes.c_uint(0), ctypes.c_ulonglong(0), ctypes.c_uint(0)
+        while not self._stop.is_set():
+            self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz))
+            self.reason_fn(self.handle, ctypes.byref(reasons))
+            self.nvml.nvmlDeviceGetPowerUsage(self.handle, ctypes.byref(mw))
+            self.samples.append((time.perf_counter(), float(mhz.value), int(reasons.value), mw.value / 1e3))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        import threading
+        self.nvml = self._open()
+        if self.nvml is not None:
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.nvml is not None:
+            self._stop.set()
+            self._thread.join()
+            # one more sample after the region, so even a region shorter than the
+            # period has its closing sample
+            if self.log_path:
+                with open(self.log_path, "w") as f:
+                    f.write("t_s,sm_mhz,reasons_mask,power_w\n")
+                    for t, m, r, w in self.samples:
+                        f.write(f"{t:.6f},{m:.0f},{r:#x},{w:.1f}\n")
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = set()
+        for _, _, mask, _ in self.samples:
+            for bit, name in self.REASONS.items():
+                if mask & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([m for _, m, _, _ in self.samples])),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "power_w_max": max(w for _, _, _, w in self.samples),
+                "samples": len(self.samples), "source": "NVML, 2 ms period"}
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
+    """Time the fp64 oracle on a bounded, seeded sample of the workload's rows.
+    Returns (TFLOP/s, rows, seconds, cores)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    total_rows = w.B * w.H * w.M
+    rows = np.sort(rng.choice(total_rows, size=64, replace=False))
+    oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, rows[:8])  # warm (build, pages)
+    n = 64
+    while True:
+        rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, rows)
+        dt = time.perf_counter() - t0
+        if dt >= seconds_target or n >= total_rows:
+            break
+        n = min(total_rows, int(n * max(2.0, 1.2 * seconds_target / max(dt, 1e-3))))
+    i = rows % w.M
+    nvis = np.minimum(i + 1, w.N) if w.causal else np.full(rows.shape, w.N)
+    flops = float(np.sum(4.0 * w.D * nvis))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    omp = os.environ.get("OMP_NUM_THREADS")
+    cores = int(omp) if omp else cores
+    return flops / dt / 1e12, int(n), dt, cores
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = si.WORKLOADS[WORKLOAD]
+    q, k, v = si.make_qkv(w)
+    per_step = []
+    for step in range(args.warmup + args.steps):
+        tf, n, dt, cores = oracle_sample(w, q, k, v, seconds_target=2.0, seed=step)
+        if step >= args.warmup:
+            per_step.append((tf, n, dt))
+    value = float(np.mean([p[0] for p in per_step]))
+    ms = float(np.mean([p[2] for p in per_step])) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "M": w.M, "N": w.N, "D": w.D,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {per_step[-1][1]} seeded random query rows of the "
+                                   f"workload (fp64, all their visible keys), ~2 s of CPU work"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_e2e(args, w, q, k, v, tq, tk, tv, o, lse, step, stream, world):
+    """Same metric end to end: each step copies Q, K, V from pinned host memory,
+    runs the forward through the C ABI and copies O and L back to pinned host
+    memory, all inside the timed region."""
+    import torch
+    hq, hk, hv = (torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+                  for a in (q, k, v))
+    ho = torch.empty(o.shape, dtype=torch.int16).pin_memory()
+    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    dq, dk, dv = tq.view(torch.int16), tk.view(torch.int16), tv.view(torch.int16)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o.view(torch.int16), non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    return {"value": w.flops * args.steps * world / t_e2e / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": int(sum(a.nbytes for a in (q, k, v))),
+            "d2h_bytes_per_step": int(o.numel() * o.element_size() + lse.numel() * 4),
+            "ms_per_step": t_e2e / args.steps * 1e3}
+
+
+# ------------------------------------------------------------------ GPU path
+def run_ours(args, rank, local, world):
+    import torch
+    import exact_attention_forward_fa2_gb300 as fa2
+
+    w = si.WORKLOADS[WORKLOAD]
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    q, k, v = si.make_qkv(w)
+    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
+    o = torch.empty_like(tq)
+    lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa2.fa2_fwd(tq, tk, tv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fa2.fa2_device_status(reset=True) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local, args.clock_log) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (outside the event pair)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    status = fa2.fa2_device_status(reset=True)
+    t_total = max_over_ranks(sum(kernel_ms) / 1e3, world)
+    value = w.flops * args.steps * world / t_total / 1e12
+    ms_per_step = t_total / args.steps * 1e3
+
+    e2e = measure_e2e(args, w, q, k, v, tq, tk, tv, o, lse, step, stream, world) if args.e2e else None
+
+    if rank != 0:
+        return
+    peak, hbm_peak, peak_kind = measured_peaks()
+    achieved = w.flops / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "M": w.M, "N": w.N, "D": w.D,
+                   "causal": w.causal, "scale": w.scale,
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
+                     "traffic": dram_traffic_per_launch(), "kernel": KERNEL,
+                     "algorithmic_flops_per_launch": w.flops,
+                     "hbm_algorithmic_bytes_per_launch": w.io_bytes(),
+                     "hbm_gbs_at_this_time": w.io_bytes() / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e9,
+                     "hbm_peak_gbs": hbm_peak},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "device_status": status,
+        "wall_s_timed_region": wall,
+    }
+    if args.cpu_baseline:
+        tf, n, dt, cores = oracle_sample(w, q, k, v, seconds_target=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{n} seeded random query rows of the workload (fp64, all "
+                                          f"their visible keys) in {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--clock-log", default=None, help="write the NVML clock samples here (CSV)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    rank, local, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, local, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,132 @@
+"""FlashAttention-2 forward pass on GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/fa2.h`` (library
+``libfa2_gb300.so``, built in-tree by ``_build.build()``).  This module only
+marshals arguments: every step of the forward pass runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing, every call raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+FA2_BF16 = 0
+FA2_FP32 = 1
+
+FA2_OK = 0
+FA2_ERR_NULL = -1
+FA2_ERR_SHAPE = -2
+FA2_ERR_HEADDIM = -3
+FA2_ERR_DTYPE = -4
+FA2_ERR_ALIGN = -5
+FA2_ERR_SCALE = -6
+FA2_ERR_TOO_LARGE = -7
+FA2_ERR_ARCH = -8
+FA2_ERR_CUDA = -9
+FA2_ERR_DEVICE_TIMEOUT = -10
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa2_gb300.so")
+
+# Every symbol include/fa2.h declares, with its ctypes signature.
+_VP, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "fa2_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP], _I),
+    "fa2_strerror": ([_I], ctypes.c_char_p),
+    "fa2_device_status": ([_I, ctypes.POINTER(_I)], _I),
+    "fa2_version": ([], _I),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Fa2Error(RuntimeError):
+    """A nonzero status returned by the library."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {fa2_strerror(code)} ({code})")
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+    return _lib
+
+
+def fa2_strerror(code: int) -> str:
+    return lib().fa2_strerror(int(code)).decode()
+
+
+def fa2_version() -> int:
+    return lib().fa2_version()
+
+
+def fa2_device_status(reset: bool = True) -> int:
+    """Raw device status word (0 = no pipeline wait ran out); clears it if ``reset``."""
+    raw = ctypes.c_int(0)
+    rc = lib().fa2_device_status(1 if reset else 0, ctypes.byref(raw))
+    if rc not in (FA2_OK, FA2_ERR_DEVICE_TIMEOUT):
+        raise Fa2Error(rc, "fa2_device_status")
+    return raw.value
+
+
+def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,
+            stream=None):
+    """FlashAttention-2 forward on torch CUDA tensors.
+
+    q [B,H,M,D], k and v [B,H,N,D] (bf16 or fp32, contiguous, same device); o
+    [B,H,M,D] and lse [B,H,M] fp32 are allocated when not given.  ``scale``
+    defaults to 1/sqrt(D).  Launches on ``stream`` (default: torch's current
+    stream) and returns (o, lse) without synchronising.
+    """
+    import torch
+
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or q.shape[:2] != k.shape[:2] \
+            or q.shape[3] != k.shape[3]:
+        raise ValueError("expected q [B,H,M,D] and k, v [B,H,N,D]")
+    B, H, M, D = q.shape
+    N = k.shape[2]
+    if q.dtype == torch.bfloat16:
+        dtype = FA2_BF16
+    elif q.dtype == torch.float32:
+        dtype = FA2_FP32
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    for t in (q, k, v):
+        if t.dtype != q.dtype or t.device != q.device or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype and device")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("o must be a contiguous tensor like q")
+    if lse.shape != (B, H, M) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 tensor of shape [B,H,M]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        rc = lib().fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           B, H, M, N, D, float(scale), 1 if causal else 0, dtype, handle)
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_fwd")
+    return o, lse

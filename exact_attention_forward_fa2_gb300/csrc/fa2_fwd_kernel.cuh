@@ -1,0 +1,562 @@
+// FlashAttention-2 forward kernel for sm_103a (GB300).
+//
+// What it computes: for one (batch, head) and a pair of 128-row query tiles,
+// the score block S = Q K_j^T against every visible key tile K_j, folded into a
+// running online softmax (row max m, row sum l, rescale of the unnormalised O by
+// exp(m_old - m_new)), O += P V_j, one divide by l at the end, and the row
+// logsumexp L = m + log l.  ("From FlashAttention to FlashAttention 2",
+// FlashAttention 2: What Changed and Layers 5-6; "FlashAttention-2 from PyTorch
+// to Triton", the Triton kernel's inner loop; "Writing FlashAttention 2 in
+// Triton", Steps 3-5.)
+//
+// How it maps to the GB300 SM (one CTA per SM, warp-specialised):
+//   warps 0..4*kQTiles-1  softmax warpgroups; warpgroup t owns query tile t,
+//                         thread r owns row r = TMEM lane r (the pages' "warps
+//                         split along Q rows only", taken to one row per thread)
+//   warp  4*kQTiles       MMA issuer (one thread): tcgen05.mma S = Q K^T into TMEM
+//                         and O += P V with P read from TMEM
+//   warp  4*kQTiles+1     TMA producer (one thread): Q once, K/V through
+//                         kStages-deep rings guarded by mbarriers
+// Shared-memory tiles are written by TMA with a 128-byte swizzle; fp32 V tiles
+// (the B operand of P V, read MN-major as TF32) use the swizzle of 32-byte chunks
+// that the tensor core expects for 32-bit MN-major operands.
+// TMEM columns: S_t at [t*128, t*128+128) (P overwrites it in place), O_t at
+// [kQTiles*128 + t*D, ... + D).  With two query tiles the MMA warp alternates
+// between them, so one tile's softmax overlaps the other tile's two GEMMs.
+//
+// Every mbarrier wait is bounded in time; a wait that runs out records an error
+// code in a device status word, sets a CTA-local abort flag, and all roles wind
+// down: in-flight copies and MMAs are waited for (again bounded), TMEM is freed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace fa2 {
+
+// Arguments that are not tensor maps.
+struct FwdParams {
+  float* lse;           // [BH, M] fp32, written for rows < M
+  int* status;          // sticky device status word (0 = ok)
+  int M, N, BH;
+  int num_units;        // BH * ceil(M / (kQTiles * 128))
+  int units_per_head;   // ceil(M / (kQTiles * 128))
+  float scale_log2;     // softmax scale * log2(e)
+};
+
+// Device status codes (first failing wait site wins).
+enum : int {
+  kStatusOk = 0,
+  kStatusTimeoutTmaK = 1,
+  kStatusTimeoutTmaV = 2,
+  kStatusTimeoutMmaQ = 3,
+  kStatusTimeoutMmaK = 4,
+  kStatusTimeoutMmaV = 5,
+  kStatusTimeoutMmaP = 6,
+  kStatusTimeoutSoftmaxS = 7,
+  kStatusTimeoutSoftmaxO = 8,
+  kStatusTimeoutEpilogue = 9,
+};
+
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s; a real wait lasts microseconds
+
+template <int D_, bool kBF16_, int kQTiles_, int kStages_>
+struct FwdCfg {
+  static constexpr int D = D_;
+  static constexpr bool kBF16 = kBF16_;
+  static constexpr int kQTiles = kQTiles_;
+  static constexpr int kStages = kStages_;
+  static constexpr int BM = 128;  // query rows per tile = TMEM lanes = MMA M
+  static constexpr int BN = 128;  // keys per tile = MMA N of S
+  static constexpr int kElem = kBF16 ? 2 : 4;
+  static constexpr int kSwElems = 128 / kElem;              // elements in one 128-byte row
+  static constexpr int kColBlocks = D / kSwElems;           // 128-byte column blocks per row
+  static constexpr int kBlockBytes = 128 * 128;             // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kColBlocks * kBlockBytes;
+  static constexpr int kMmaK = 32 / kElem;                  // one MMA consumes 32 bytes of K
+  static constexpr int kStepsS = D / kMmaK;
+  static constexpr int kStepsPV = BN / kMmaK;
+  static constexpr int kPCols = kBF16 ? BN / 2 : BN;        // TMEM columns holding P
+  static constexpr int kSoftmaxWarps = 4 * kQTiles;
+  static constexpr int kMmaWarp = kSoftmaxWarps;
+  static constexpr int kTmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kColS(int t) { return t * BN; }
+  static constexpr int kColO(int t) { return kQTiles * BN + t * D; }
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kNumBars = 4 * kQTiles + 4 * kStages + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // barrier indices
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarKFull = kBarQ + kQTiles;
+  static constexpr int kBarKEmpty = kBarKFull + kStages;
+  static constexpr int kBarVFull = kBarKEmpty + kStages;
+  static constexpr int kBarVEmpty = kBarVFull + kStages;
+  static constexpr int kBarSFull = kBarVEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + kQTiles;
+  static constexpr int kBarOFull = kBarPFull + kQTiles;
+  static constexpr int kBarMmaDone = kBarOFull + kQTiles;
+  static constexpr uint32_t kIdescS = ptx::make_idesc(kBF16, false, BM, BN);
+  static constexpr uint32_t kIdescPV = ptx::make_idesc(kBF16, true, BM, D);
+
+  static_assert(D % kSwElems == 0, "head dim must fill whole 128-byte rows");
+  static_assert(kQTiles * (BN + D) <= 512, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kStepsS % 4 == 0 || kStepsS < 4, "K steps per 128-byte block");
+};
+
+// Work decode and per-tile key-tile counts (shared by all roles).
+struct Unit {
+  int bh;    // flattened batch * heads index
+  int pair;  // which group of kQTiles query tiles within the head
+};
+
+// Causal units are launched longest first (largest query offset, heads
+// interleaved) so the tail of the grid holds the short ones; non-causal units
+// keep one head's query tiles adjacent so its K/V stay hot in L2.
+__device__ __forceinline__ Unit unit_of_block(const FwdParams& p, bool causal) {
+  Unit u;
+  const int b = static_cast<int>(blockIdx.x);
+  if (causal) {
+    u.pair = p.units_per_head - 1 - b / p.BH;
+    u.bh = b % p.BH;
+  } else {
+    u.bh = b / p.units_per_head;
+    u.pair = b % p.units_per_head;
+  }
+  return u;
+}
+
+// Number of key tiles query tile starting at row0 must visit (0 = tile empty).
+__device__ __forceinline__ int kv_tiles_for(int row0, int M, int N, bool causal) {
+  if (row0 >= M) return 0;
+  const int total = (N + 127) / 128;
+  if (!causal) return total;
+  const int last_row = min(row0 + 128, M) - 1;
+  return min(total, last_row / 128 + 1);
+}
+
+struct WaitCtx {
+  volatile uint32_t* abort_flag;  // CTA-local
+  int* status;                    // device-wide sticky status
+};
+
+// Bounded mbarrier wait.  False if the CTA is aborting or the wait ran out.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                             int code) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*w.abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        *w.abort_flag = 1u;
+        atomicCAS(w.status, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Wind-down wait: ignores the abort flag, bounded in time only.
+__device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (ptx::globaltimer_ns() - t0 > kWaitTimeoutNs) return;
+  }
+}
+
+template <class C, bool kCausal>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const FwdParams p) {
+  using namespace ptx;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::kOffMisc);
+  // misc[0] TMEM base address, misc[1] abort flag, misc[2] status at CTA start
+
+  const int warp = static_cast<int>(threadIdx.x) / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+  auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  const Unit unit = unit_of_block(p, kCausal);
+  const int bh = unit.bh;
+  int row0[C::kQTiles], nkv[C::kQTiles];
+  int n_max = 0;
+#pragma unroll
+  for (int t = 0; t < C::kQTiles; ++t) {
+    row0[t] = (unit.pair * C::kQTiles + t) * C::BM;
+    nkv[t] = kv_tiles_for(row0[t], p.M, p.N, kCausal);
+    n_max = max(n_max, nkv[t]);
+  }
+
+  // ------------------------------------------------------------ set-up
+  if (threadIdx.x == 0) {
+    misc[1] = 0u;
+    misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
+    for (int t = 0; t < C::kQTiles; ++t) {
+      mbar_init(bar(C::kBarQ + t), 1);
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarOFull + t), 1);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarKFull + s), 1);
+      mbar_init(bar(C::kBarKEmpty + s), 1);
+      mbar_init(bar(C::kBarVFull + s), 1);
+      mbar_init(bar(C::kBarVEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarMmaDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kTmaWarp && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmO);
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(base + C::kOffMisc, C::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = misc[0];
+  const bool skip = misc[2] != 0u;  // an earlier launch failed: do nothing
+  const WaitCtx wctx{misc + 1, p.status};
+
+  if (!skip && warp == C::kTmaWarp) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+#pragma unroll
+      for (int t = 0; t < C::kQTiles; ++t) {
+        if (nkv[t] == 0) continue;
+        mbar_arrive_expect_tx(bar(C::kBarQ + t), C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ,
+                           bar(C::kBarQ + t), cb * C::kSwElems, row0[t], bh, pol_q);
+      }
+      int issued = 0;  // K/V tiles whose loads were issued
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t use = static_cast<uint32_t>(j / C::kStages);
+        if (use > 0 && !wait_bounded(bar(C::kBarKEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaK))
+          break;
+        mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_load_3d_hint(base + C::kOffK + s * C::kTileBytes + cb * C::kBlockBytes, &tmK,
+                           bar(C::kBarKFull + s), cb * C::kSwElems, j * C::BN, bh, pol_kv);
+        if (use > 0 && !wait_bounded(bar(C::kBarVEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaV)) {
+          issued = -(j + 1);  // K_j issued, V_j not
+          break;
+        }
+        mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_load_3d_hint(base + C::kOffV + s * C::kTileBytes + cb * C::kBlockBytes, &tmV,
+                           bar(C::kBarVFull + s), cb * C::kSwElems, j * C::BN, bh, pol_kv);
+        issued = j + 1;
+      }
+      if (*wctx.abort_flag) {
+        // wind down: every issued copy must land before the CTA's smem is released
+        const int k_done = issued >= 0 ? issued : -issued;
+        const int v_done = issued >= 0 ? issued : -issued - 1;
+        for (int t = 0; t < C::kQTiles; ++t)
+          if (nkv[t] > 0) drain_bounded(bar(C::kBarQ + t), 0);
+        for (int j = max(0, k_done - C::kStages); j < k_done; ++j)
+          drain_bounded(bar(C::kBarKFull + j % C::kStages), (j / C::kStages) & 1);
+        for (int j = max(0, v_done - C::kStages); j < v_done; ++j)
+          drain_bounded(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (!skip && warp == C::kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < C::kQTiles; ++t)
+        if (ok && nkv[t] > 0) ok = wait_bounded(bar(C::kBarQ + t), 0, wctx, kStatusTimeoutMmaQ);
+      for (int j = 0; ok && j <= n_max; ++j) {
+        const int s = j % C::kStages;
+        bool v_ready = false, k_ready = false;
+#pragma unroll
+        for (int t = 0; t < C::kQTiles; ++t) {
+          if (j >= 1 && j - 1 < nkv[t]) {
+            // O_t += P_t V_{j-1}
+            const int jp = j - 1;
+            const int sv = jp % C::kStages;
+            ok = wait_bounded(bar(C::kBarPFull + t), jp & 1, wctx, kStatusTimeoutMmaP);
+            if (!ok) break;
+            if (!v_ready) {
+              ok = wait_bounded(bar(C::kBarVFull + sv), (jp / C::kStages) & 1, wctx, kStatusTimeoutMmaV);
+              if (!ok) break;
+              v_ready = true;
+            }
+            tc_fence_after_sync();
+            const uint32_t v_base = base + C::kOffV + sv * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < C::kStepsPV; ++kk) {
+              // B = V rows [kk*kMmaK, +kMmaK), all D columns, MN-major
+              const uint64_t bdesc =
+                  C::kBF16 ? smem_desc(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 1024, kLayoutSw128)
+                           : smem_desc(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 512, kLayoutSw128Atom32);
+              const uint32_t a_tmem = tmem + C::kColS(t) + kk * 8;
+              if constexpr (C::kBF16)
+                mma_f16_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
+              else
+                mma_tf32_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar(C::kBarOFull + t));
+          }
+          if (j < nkv[t]) {
+            // S_t = Q_t K_j^T
+            if (!k_ready) {
+              ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
+              if (!ok) break;
+              k_ready = true;
+              tc_fence_after_sync();
+            }
+            const uint32_t q_base = base + C::kOffQ + t * C::kTileBytes;
+            const uint32_t k_base = base + C::kOffK + s * C::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < C::kStepsS; ++kk) {
+              const uint32_t off = (kk / 4) * C::kBlockBytes + (kk % 4) * 32;
+              const uint64_t adesc = smem_desc_sw128(q_base + off, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(k_base + off, 16, 1024);
+              if constexpr (C::kBF16)
+                mma_f16_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+              else
+                mma_tf32_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bar(C::kBarSFull + t));
+          }
+        }
+        if (!ok) break;
+        if (j >= 1) tc_commit(bar(C::kBarVEmpty + (j - 1) % C::kStages));
+        if (j < n_max) tc_commit(bar(C::kBarKEmpty + s));
+      }
+      // every MMA issued above must finish before TMEM is released
+      tc_commit(bar(C::kBarMmaDone));
+      drain_bounded(bar(C::kBarMmaDone), 0);
+    }
+    __syncwarp();
+  } else if (!skip && warp < C::kSoftmaxWarps) {
+    // ---------------------------------------------------------- softmax warpgroups
+    const int t = warp / 4;
+    const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
+    const int tile_row0 = (unit.pair * C::kQTiles + t) * C::BM;
+    const int row = tile_row0 + r;
+    const int n_t = kv_tiles_for(tile_row0, p.M, p.N, kCausal);
+    const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + C::kColS(t);
+    const uint32_t tO = tmem + lane_addr + C::kColO(t);
+    const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+    float m_run = -INFINITY;  // exponent base in use: a running max of scale*log2e*s
+    float l_run = 0.f;        // running sum of the rounded exp2(s*sl2 - m_run)
+    bool ok = n_t > 0;
+
+    for (int j = 0; ok && j < n_t; ++j) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + t), j & 1, wctx, kStatusTimeoutSoftmaxS));
+      if (!ok) break;
+      tc_fence_after_sync();
+      // the whole S row of this thread: four TMEM loads in flight, one wait
+      uint32_t v[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld_x32(tS + ch * 32, v[ch]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) reg_fence_x32(v[ch]);
+      float s[C::BN];
+#pragma unroll
+      for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
+      // mask keys past N and, when causal, keys after this row (boundary tiles only)
+      const int key0 = j * C::BN;
+      const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
+      if (boundary) {
+        int lim = p.N - 1 - key0;
+        if (kCausal) lim = min(lim, row - key0);
+#pragma unroll
+        for (int c = 0; c < C::BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+      }
+      // row max: four independent chains of 3-input max
+      float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int c = 4; c < C::BN; c += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], s[c + q], s[c + 4 + q]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+      const float m_new = fmaxf(m_run, m_tile);
+      // Move the exponent base only when the max grew by more than 8 (factor 256):
+      // the result is exact for any base, and skipping the rescale keeps O in TMEM
+      // untouched on most tiles.  (-inf) - (-inf) is NaN, so an empty row stays put.
+      const bool rescale = (m_new - m_run) > 8.0f;
+      const float m_use = rescale ? m_new : m_run;
+      const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.0f;
+      const float neg_base = (m_use == -INFINITY) ? 0.f : -m_use;
+      const uint64_t nb2 = pack_f32x2(neg_base, neg_base);
+      // P = exp2(s*sl2 - base), rounded to the P.V operand type.  l sums the
+      // rounded values, so O = sum(P v) / sum(P) is an exact convex combination
+      // of V rows with the weights the tensor core actually used.
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // packed pairs of partial sums
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // two halves of 64 keys
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = h * 64 + 2 * i;
+          float x0, x1;
+          unpack_f32x2(ffma2(pack_f32x2(s[c], s[c + 1]), sl2x2, nb2), x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if constexpr (C::kBF16) {
+            const uint32_t w = pack_bf16x2(p0, p1);
+            pk[i] = w;
+            acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(__uint_as_float(w << 16),
+                                                      __uint_as_float(w & 0xffff0000u)));
+          } else {
+            const uint32_t r0 = round_tf32(p0), r1 = round_tf32(p1);
+            s[c] = __uint_as_float(r0);
+            s[c + 1] = __uint_as_float(r1);
+            acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(s[c], s[c + 1]));
+          }
+        }
+        if constexpr (C::kBF16) {
+          tmem_st_x32(tS + h * 32, pk);  // 64 keys -> 32 columns of bf16x2
+        } else {
+          uint32_t q0[32], q1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            q0[i] = __float_as_uint(s[h * 64 + i]);
+            q1[i] = __float_as_uint(s[h * 64 + 32 + i]);
+          }
+          tmem_st_x32(tS + h * 64, q0);
+          tmem_st_x32(tS + h * 64 + 32, q1);
+        }
+      }
+      float a0, a1, a2, a3, a4, a5, a6, a7;
+      unpack_f32x2(acc[0], a0, a1);
+      unpack_f32x2(acc[1], a2, a3);
+      unpack_f32x2(acc[2], a4, a5);
+      unpack_f32x2(acc[3], a6, a7);
+      l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O_t *= alpha once P_{j-1} V_{j-1} has landed in TMEM
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(bar(C::kBarOFull + t), (j - 1) & 1, wctx, kStatusTimeoutSoftmaxO));
+        if (!ok) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + ch * 32, o);
+          tmem_ld_wait();
+          reg_fence_x32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x32(tO + ch * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::kBarPFull + t));
+      m_run = m_use;
+    }
+
+    // ------------------------------------------------------------ epilogue
+    if (n_t > 0) {
+      if (ok)
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
+                                                  kStatusTimeoutEpilogue));
+      // Q_t's shared tile is free once the last GEMM of this tile completed: stage O there
+      const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
+      if (ok) {
+        tc_fence_after_sync();
+        const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+#pragma unroll
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_x32(tO + ch * 32, v);
+          tmem_ld_wait();
+          reg_fence_x32(v);
+          if constexpr (C::kBF16) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunks of 8 bf16
+              const int cidx = ch * 4 + q4;
+              const int cb = cidx / 8, c = cidx % 8;
+              const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * inv_l,
+                                   __uint_as_float(v[q4 * 8 + 2 * e + 1]) * inv_l);
+              st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+            }
+          } else {
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {  // 16-byte chunks of 4 fp32
+              const int cb = ch, c = q8;
+              const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+              st_shared_v4(addr, __float_as_uint(__uint_as_float(v[q8 * 4 + 0]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[q8 * 4 + 1]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[q8 * 4 + 2]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[q8 * 4 + 3]) * inv_l));
+            }
+          }
+        }
+        if (row < p.M) {
+          // L = ln(2) * (m + log2 l): the base-2 running state converted to natural log
+          const float L = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
+          p.lse[static_cast<int64_t>(bh) * p.M + row] = L;
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1 + t, 128);
+      if (r == 0 && *wctx.abort_flag == 0u) {
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh);
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Host-side launch description shared by the instantiation units.
+struct FwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmO;
+  FwdParams params;
+  int causal;
+  cudaStream_t stream;
+};
+
+}  // namespace fa2

@@ -1,0 +1,99 @@
+/*
+ * fa2.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 forward library
+ * (libfa2_gb300.so).
+ *
+ * The operation ("From FlashAttention to FlashAttention 2", FlashAttention 2:
+ * What Changed and Layer 5: The Forward Kernel; "FlashAttention-2 from PyTorch
+ * to Triton", introduction and the Triton kernel; "Writing FlashAttention 2 in
+ * Triton", Steps 1-6): for every batch b, head h and query row i,
+ *     O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) v_j
+ *     L[b,h,i]   = log sum_j exp(scale * q_i . k_j)        (natural log)
+ * over the visible keys j: j < N, and j <= i when causal (top-left aligned,
+ * "Writing FlashAttention 2 in Triton", Step 4).  The library computes it tile by
+ * tile with the online-softmax recurrence and never forms the N x N scores.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named q, k, v, o, lse are DEVICE pointers on the current CUDA
+ *     device, owned by the caller, which allocates and frees them.  The library
+ *     allocates no device memory, keeps no pointer after the call returns and
+ *     never synchronises the stream.
+ *   - Layouts are contiguous row-major: q and o are [B, H, M, D], k and v are
+ *     [B, H, N, D] (the problem statement of the pages: Q [B,H,M,D], K/V
+ *     [B,H,N,D], O [B,H,M,D]); lse is [B, H, M] fp32.  Element type of q, k, v, o
+ *     is `dtype`: FA2_BF16 (bfloat16) or FA2_FP32 (fp32 storage; the products run
+ *     on the tensor cores as TF32 with fp32 accumulation).
+ *   - q, k, v and o must be 16-byte aligned (TMA); lse 4-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  A return of FA2_OK means the kernel was launched; results are
+ *     valid once the stream has reached that point.
+ *   - Errors are returned as negative status codes; nothing is launched on
+ *     error.  No exception crosses the ABI and the library never exits the
+ *     process.  fa2_strerror() names each code.
+ */
+#ifndef FA2_GB300_H
+#define FA2_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types of q, k, v and o. */
+#define FA2_BF16 0
+#define FA2_FP32 1
+
+/* Status codes. */
+#define FA2_OK 0
+#define FA2_ERR_NULL (-1)           /* a required pointer is NULL */
+#define FA2_ERR_SHAPE (-2)          /* B, H, M or N <= 0 */
+#define FA2_ERR_HEADDIM (-3)        /* D is not 64 or 128 */
+#define FA2_ERR_DTYPE (-4)          /* dtype is not FA2_BF16 or FA2_FP32 */
+#define FA2_ERR_ALIGN (-5)          /* q/k/v/o not 16-byte or lse not 4-byte aligned */
+#define FA2_ERR_SCALE (-6)          /* scale is not finite and > 0 */
+#define FA2_ERR_TOO_LARGE (-7)      /* sizes exceed the grid or tensor-map limits */
+#define FA2_ERR_ARCH (-8)           /* current device is not compute capability 10.3 */
+#define FA2_ERR_CUDA (-9)           /* a CUDA runtime or driver call failed */
+#define FA2_ERR_DEVICE_TIMEOUT (-10) /* a kernel gave up on a pipeline wait (see fa2_device_status) */
+
+/*
+ * fa2_fwd -- FlashAttention-2 forward pass.
+ *
+ * Computes O and L as defined above for all B*H heads.
+ *   q      [B,H,M,D] queries            k, v  [B,H,N,D] keys and values
+ *   o      [B,H,M,D] output (written)   lse   [B,H,M] fp32 logsumexp (written)
+ *   B, H   batch size and number of heads (> 0)
+ *   M, N   query and key sequence lengths (> 0, any value: ragged tails are
+ *          masked, "FlashAttention-2 from PyTorch to Triton", the ragged-tile fix)
+ *   D      head dimension: 64 or 128
+ *   scale  softmax scale applied to q.k, finite and > 0 (usually 1/sqrt(D))
+ *   causal 0: every key visible; nonzero: key j visible to query i iff j <= i
+ *   dtype  FA2_BF16 or FA2_FP32
+ *   stream cudaStream_t to launch on
+ * Returns FA2_OK or a negative FA2_ERR_* code.  Inputs are only read; o and lse
+ * are fully overwritten (rows i < M only; memory past the tensors is untouched).
+ */
+int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+            int M, int N, int D, float scale, int causal, int dtype, void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* fa2_strerror(int status);
+
+/*
+ * fa2_device_status -- read the sticky device-side status word of the current
+ * device.  Every pipeline wait inside the kernels is bounded; a wait that runs
+ * out records a nonzero code here (the first one wins) and the kernel winds down
+ * without hanging.  While the word is nonzero, later launches on that device
+ * return at once without computing.  This call synchronises the device, returns
+ * FA2_OK if the word is zero and FA2_ERR_DEVICE_TIMEOUT otherwise (or
+ * FA2_ERR_CUDA if it cannot be read), stores the raw word in *raw_code when
+ * raw_code is not NULL, and clears the word when `reset` is nonzero.
+ */
+int fa2_device_status(int reset, int* raw_code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_GB300_H */

@@ -1,0 +1,89 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/fa2.h declares, and rejects bad arguments before any CUDA work.
+No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_fa2_gb300 as fa2
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa2.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa2_\w+)\s*\(", text, flags=re.M)))
+
+
+def declared_codes():
+    return {m.group(1): int(m.group(2)) for m in
+            re.finditer(r"#define\s+(FA2_\w+)\s+\(?(-?\d+)\)?", open(HEADER).read())}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_forward_fa2_gb300 import _build
+    _build.build()
+    return fa2.lib()
+
+
+def test_header_declares_the_api():
+    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_strerror", "fa2_version"]
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in fa2.SIGNATURES
+
+
+def test_binding_constants_match_header():
+    for name, value in declared_codes().items():
+        assert getattr(fa2, name) == value, name
+
+
+def test_strerror_names_every_code(lib):
+    codes = declared_codes()
+    msgs = set()
+    for name, value in codes.items():
+        if name in ("FA2_BF16", "FA2_FP32"):
+            continue
+        msg = fa2.fa2_strerror(value)
+        assert msg and msg != "unknown status", name
+        msgs.add(msg)
+    assert fa2.fa2_strerror(12345) == "unknown status"
+    assert fa2.fa2_version() >= 100
+
+
+# Fake, 16-byte aligned addresses: validation must fail before anything touches them.
+P = 0x10000
+
+
+def call(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, M=8, N=8, D=64, scale=0.125, causal=0, dtype=0):
+    return lib.fa2_fwd(q, k, v, o, lse, B, H, M, N, D, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa2.FA2_ERR_NULL), (dict(k=None), fa2.FA2_ERR_NULL), (dict(v=None), fa2.FA2_ERR_NULL),
+    (dict(o=None), fa2.FA2_ERR_NULL), (dict(lse=None), fa2.FA2_ERR_NULL),
+    (dict(B=0), fa2.FA2_ERR_SHAPE), (dict(H=-1), fa2.FA2_ERR_SHAPE), (dict(M=0), fa2.FA2_ERR_SHAPE),
+    (dict(N=0), fa2.FA2_ERR_SHAPE),
+    (dict(D=32), fa2.FA2_ERR_HEADDIM), (dict(D=96), fa2.FA2_ERR_HEADDIM), (dict(D=256), fa2.FA2_ERR_HEADDIM),
+    (dict(dtype=2), fa2.FA2_ERR_DTYPE), (dict(dtype=-1), fa2.FA2_ERR_DTYPE),
+    (dict(scale=0.0), fa2.FA2_ERR_SCALE), (dict(scale=-1.0), fa2.FA2_ERR_SCALE),
+    (dict(scale=float("inf")), fa2.FA2_ERR_SCALE), (dict(scale=float("nan")), fa2.FA2_ERR_SCALE),
+    (dict(q=P + 8), fa2.FA2_ERR_ALIGN), (dict(o=P + 2), fa2.FA2_ERR_ALIGN), (dict(lse=P + 2), fa2.FA2_ERR_ALIGN),
+    (dict(B=65536, H=65536), fa2.FA2_ERR_TOO_LARGE),
+])
+def test_rejects_bad_arguments(lib, kw, code):
+    assert call(lib, **kw) == code
+
+
+def test_no_gpu_means_an_error_not_a_fallback(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call(lib) in (fa2.FA2_ERR_CUDA, fa2.FA2_ERR_ARCH)

@@ -1,0 +1,183 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
+the same seeded inputs.  Bar: |dL| <= 1e-2 for bf16 and <= 5e-3 for fp32
+inputs (TF32 tensor-core products); |dO| within the same bound on top of the
+rounding of the exact O to the output type (half a bf16 ulp of O; see
+gpu_helpers.compare), over every compared element.
+
+Shapes cover several 128-row tiles with ragged tails on both axes, the pages'
+test shapes ("FlashAttention-2 from PyTorch to Triton", the test file; "Writing
+FlashAttention 2 in Triton", numerics harness), degenerate sizes (one query,
+one key), non-square causal in both directions, and the five full-size
+workloads (full oracle comparison where the oracle finishes in seconds,
+sampled rows for the 8192 x 8192 ones).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_helpers import TOL, compare, sample_rows, to_device, to_host_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fa2():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_forward_fa2_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.fixture(autouse=True)
+def device_status_clean(fa2):
+    assert fa2.fa2_device_status(reset=True) == 0
+    yield
+    assert fa2.fa2_device_status(reset=True) == 0, "a kernel pipeline wait ran out"
+
+
+DEV = "cuda:0"
+
+
+def run_gpu(fa2, q, k, v, scale, causal):
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    o, lse = fa2.fa2_fwd(tq, tk, tv, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    return to_host_f64(o), lse.cpu().numpy().astype(np.float64)
+
+
+def inputs(seed, B, H, M, N, D, dtype, sigma_qk=1.0):
+    q = si.normal(seed, 1, (B, H, M, D), sigma_qk, dtype)
+    k = si.normal(seed, 2, (B, H, N, D), sigma_qk, dtype)
+    v = si.normal(seed, 3, (B, H, N, D), 1.0, dtype)
+    return q, k, v
+
+
+SMALL = [  # (B, H, M, N, D)
+    (4, 1, 128, 128, 64),     # the assignment's shape (batch*heads flattened)
+    (2, 1, 1024, 1024, 64),
+    (2, 1, 100, 100, 64),     # ragged last tile on both axes
+    (1, 1, 200, 96, 128),
+    (1, 8, 512, 512, 64),
+    (1, 1, 1, 1, 64),         # one query, one key
+    (1, 2, 1, 1000, 128),     # one query
+    (2, 1, 1000, 1, 64),      # one key
+    (1, 1, 129, 129, 128),
+    (1, 2, 255, 257, 64),
+    (1, 1, 256, 256, 128),
+    (1, 1, 257, 128, 64),     # causal: more queries than keys
+    (1, 1, 130, 700, 128),    # causal: more keys than queries
+    (3, 5, 17, 300, 64),
+    (1, 1, 384, 640, 128),
+]
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes_all_rows(fa2, shape, causal, dtype):
+    B, H, M, N, D = shape
+    q, k, v = inputs(1000 + sum(shape), B, H, M, N, D, dtype)
+    scale = D ** -0.5
+    o, lse = run_gpu(fa2, q, k, v, scale, causal)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, scale, causal)
+    eo, el, excess = compare(o, lse, o_ref, l_ref, dtype)
+    assert excess <= 0 and el <= TOL[dtype], (eo, el)
+
+
+def test_sharp_scores_ragged(fa2):
+    """sigma_QK = 3: near one-hot rows that exercise the max rescaling."""
+    B, H, M, N, D = 2, 3, 300, 777, 128
+    q, k, v = inputs(77, B, H, M, N, D, si.BF16, sigma_qk=3.0)
+    for causal in (False, True):
+        o, lse = run_gpu(fa2, q, k, v, D ** -0.5, causal)
+        o_ref, l_ref = oracle.attn_fwd(q, k, v, D ** -0.5, causal)
+        eo, el, excess = compare(o, lse, o_ref, l_ref, si.BF16)
+        assert excess <= 0 and el <= TOL[si.BF16], (causal, eo, el)
+
+
+def test_other_scales(fa2):
+    B, H, M, N, D = 1, 2, 150, 260, 64
+    q, k, v = inputs(5, B, H, M, N, D, si.BF16)
+    for scale in (0.01, 0.5, 1.0):
+        o, lse = run_gpu(fa2, q, k, v, scale, False)
+        o_ref, l_ref = oracle.attn_fwd(q, k, v, scale, False)
+        eo, el, excess = compare(o, lse, o_ref, l_ref, si.BF16)
+        assert excess <= 0 and el <= TOL[si.BF16], (scale, eo, el)
+
+
+def test_head_dim_32_is_rejected(fa2):
+    t = torch.zeros((1, 1, 37, 32), dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros((1, 1, 53, 32), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(fa2.Fa2Error) as ei:
+        fa2.fa2_fwd(t, k, k.clone())
+    assert ei.value.code == fa2.FA2_ERR_HEADDIM
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+def test_writes_stay_inside_o_and_lse(fa2, dtype):
+    """O and L sit inside larger buffers filled with a canary; only the rows of
+    the tensors may change (TMA store clipping at ragged M, L rows < M)."""
+    B, H, M, N, D = 2, 2, 100, 300, 128
+    q, k, v = inputs(3, B, H, M, N, D, dtype)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    tdt = tq.dtype
+    pad = 4096
+    o_buf = torch.full((pad + B * H * M * D + pad,), float("nan"), dtype=tdt, device=DEV)
+    l_buf = torch.full((pad + B * H * M + pad,), -7.0, dtype=torch.float32, device=DEV)
+    o = o_buf[pad:pad + B * H * M * D].view(B, H, M, D)
+    lse = l_buf[pad:pad + B * H * M].view(B, H, M)
+    fa2.fa2_fwd(tq, tk, tv, o=o, lse=lse, causal=True)
+    torch.cuda.synchronize()
+    assert torch.isnan(o_buf[:pad]).all() and torch.isnan(o_buf[-pad:]).all()
+    assert (l_buf[:pad] == -7.0).all() and (l_buf[-pad:] == -7.0).all()
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, D ** -0.5, True)
+    eo, el, excess = compare(to_host_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, l_ref, dtype)
+    assert excess <= 0 and el <= TOL[dtype], (eo, el)
+
+
+def test_deterministic_and_stream(fa2):
+    B, H, M, N, D = 2, 4, 640, 640, 128
+    q, k, v = inputs(9, B, H, M, N, D, si.BF16)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    o1, l1 = fa2.fa2_fwd(tq, tk, tv, causal=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, l2 = fa2.fa2_fwd(tq, tk, tv, causal=True, stream=s)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+def full_or_sampled(fa2, name, sampled):
+    w = si.WORKLOADS[name]
+    q, k, v = si.make_qkv(w)
+    o, lse = run_gpu(fa2, q, k, v, w.scale, w.causal)
+    if sampled:
+        rows = sample_rows(w.B, w.H, w.M, w.N, w.causal)
+        o_ref, l_ref = oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, rows)
+        o_cmp, l_cmp = o.reshape(-1, w.D)[rows], lse.reshape(-1)[rows]
+    else:
+        o_ref, l_ref = oracle.attn_fwd(q, k, v, w.scale, w.causal)
+        o_cmp, l_cmp = o, lse
+        # every row was written: nothing left at a sentinel, all finite
+    eo, el, excess = compare(o_cmp, l_cmp, o_ref, l_ref, w.dtype)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    print(f"{name}: max|dO|={eo:.3e} max|dL|={el:.3e} excess over bound={excess:.3e}")
+    assert excess <= 0 and el <= TOL[w.dtype], (eo, el)
+
+
+@pytest.mark.parametrize("name", ["fp32_1x1x128x128x64", "tf32_4x12x2048x2048x64",
+                                  "bf16_4x16x4096x4096x64_causal", "bf16_8x32x1000x3000x128_sharp"])
+def test_workload_full(fa2, name):
+    full_or_sampled(fa2, name, sampled=False)
+
+
+@pytest.mark.parametrize("name", ["bf16_2x16x8192x8192x128", "bf16_2x16x8192x8192x128_causal"])
+def test_workload_sampled_rows(fa2, name):
+    full_or_sampled(fa2, name, sampled=True)
