@@ -85,8 +85,8 @@ struct FwdCfg {
   static constexpr int kTmaWarp = kSoftmaxWarps + 1;
   static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kColS(int t) { return t * BN; }
-  static constexpr int kColO(int t) { return kQTiles * BN + t * D; }
+  __host__ __device__ static constexpr int kColS(int t) { return t * BN; }
+  __host__ __device__ static constexpr int kColO(int t) { return kQTiles * BN + t * D; }
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
