@@ -59,16 +59,24 @@ def _bind(lib):
     lib.oracle_attn_fwd_tiled.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, dbl, i32,
                                           i32, i32, i32]
     lib.oracle_attn_fwd_tiled.restype = i32
+    lib.oracle_attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, dbl, i32,
+                                        i32]
+    lib.oracle_attn_fwd_gqa.restype = i32
+    lib.oracle_attn_fwd_gqa_rows.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32,
+                                             i32, dbl, i32, i32]
+    lib.oracle_attn_fwd_gqa_rows.restype = i32
     return lib
 
 
-def _prep(q, k, v):
+def _prep(q, k, v, gqa=False):
     q, k, v = (np.ascontiguousarray(t) for t in (q, k, v))
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPE_CODE:
         raise TypeError("q, k, v must share one dtype: uint16 (bf16 bits), float32 or float64")
-    if q.ndim != 4 or k.ndim != 4 or v.shape != k.shape or q.shape[:2] != k.shape[:2] \
+    if q.ndim != 4 or k.ndim != 4 or v.shape != k.shape or q.shape[0] != k.shape[0] \
             or q.shape[3] != k.shape[3]:
-        raise ValueError("expected q [B,H,M,D] and k, v [B,H,N,D]")
+        raise ValueError("expected q [B,H,M,D] and k, v [B,Hkv,N,D]")
+    if (not gqa and q.shape[1] != k.shape[1]) or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("k, v head count must equal (or, for grouped-query attention, divide) H")
     B, H, M, D = q.shape
     N = k.shape[2]
     return q, k, v, B, H, M, N, D, _DTYPE_CODE[q.dtype]
@@ -113,4 +121,35 @@ def attn_fwd_tiled(q, k, v, scale: float, causal: bool, block_m: int, block_n: i
                                    code, int(block_m), int(block_n))
     if rc:
         raise RuntimeError(f"oracle_attn_fwd_tiled failed: {rc}")
+    return o, lse
+
+
+def attn_fwd_gqa(q, k, v, scale: float, causal: bool, lib=None):
+    """Grouped-query attention: q [B,H,M,D], k and v [B,Hkv,N,D] with Hkv | H;
+    returns (O [B,H,M,D], L [B,H,M]) fp64."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v, gqa=True)
+    Hkv = k.shape[1]
+    o = np.empty((B, H, M, D), np.float64)
+    lse = np.empty((B, H, M), np.float64)
+    rc = lib.oracle_attn_fwd_gqa(q.ctypes.data, k.ctypes.data, v.ctypes.data, o.ctypes.data,
+                                 lse.ctypes.data, B, H, Hkv, M, N, D, float(scale), int(causal), code)
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_gqa failed: {rc}")
+    return o, lse
+
+
+def attn_fwd_gqa_rows(q, k, v, scale: float, causal: bool, rows, lib=None):
+    """Selected rows of grouped-query attention: returns (O [n,D], L [n]) fp64."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v, gqa=True)
+    Hkv = k.shape[1]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    o = np.empty((rows.size, D), np.float64)
+    lse = np.empty((rows.size,), np.float64)
+    rc = lib.oracle_attn_fwd_gqa_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                      rows.ctypes.data, rows.size, o.ctypes.data, lse.ctypes.data,
+                                      B, H, Hkv, M, N, D, float(scale), int(causal), code)
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_gqa_rows failed: {rc}")
     return o, lse

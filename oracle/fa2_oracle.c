@@ -32,6 +32,11 @@
  * kernel's arithmetic error.  Layouts: q [B,H,M,D], k and v [B,H,N,D],
  * o [B,H,M,D] fp64, lse [B,H,M] fp64, all contiguous.
  *
+ * Grouped-query attention ("From FlashAttention to FlashAttention 2", Layer 8:
+ * Multi-Query / Grouped-Query Attention): k and v hold Hkv heads, Hkv divides H,
+ * and query head h reads key/value head h / (H / Hkv) of the same batch entry.
+ * Hkv == H is ordinary multi-head attention.
+ *
  * Return value: 0 on success, -1 on invalid sizes, -2 on allocation failure,
  * -3 if a row had no visible key (cannot happen for N >= 1).
  */
@@ -51,10 +56,16 @@ static double widen(const void* base, int64_t idx, int dtype) {
   return ((const double*)base)[idx];
 }
 
-static int check_sizes(int B, int H, int M, int N, int D, int dtype) {
-  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || D <= 0) return -1;
+static int check_sizes(int B, int H, int Hkv, int M, int N, int D, int dtype) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || M <= 0 || N <= 0 || D <= 0) return -1;
+  if (H % Hkv != 0) return -1;
   if (dtype < 0 || dtype > 2) return -1;
   return 0;
+}
+
+/* Flat key/value head index read by flat query head bh = b*H + h. */
+static int64_t kv_head(int64_t bh, int H, int Hkv) {
+  return (bh / H) * Hkv + (bh % H) / (H / Hkv);
 }
 
 /* Number of keys visible to query row i. */
@@ -66,10 +77,10 @@ static int64_t visible_keys(int64_t i, int N, int causal) {
 /* One query row of one (b,h): the definition, with all scores of the row formed
  * explicitly.  w must hold N doubles. */
 static int attn_row(const void* q, const void* k, const void* v, int dtype,
-                    int64_t bh, int64_t i, int M, int N, int D, double scale,
+                    int64_t bh, int64_t kvh, int64_t i, int M, int N, int D, double scale,
                     int causal, double* o_row, double* lse, double* w) {
   const int64_t qoff = (bh * M + i) * (int64_t)D;
-  const int64_t kvoff = bh * (int64_t)N * D;
+  const int64_t kvoff = kvh * (int64_t)N * D;
   const int64_t nvis = visible_keys(i, N, causal);
   if (nvis <= 0) return -3;
 
@@ -95,11 +106,11 @@ static int attn_row(const void* q, const void* k, const void* v, int dtype,
   return 0;
 }
 
-/* Every row of every (b,h). */
-int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, double* lse,
-                    int B, int H, int M, int N, int D, double scale, int causal,
-                    int dtype) {
-  if (check_sizes(B, H, M, N, D, dtype)) return -1;
+/* Every row of every (b,h); k and v hold Hkv heads. */
+int oracle_attn_fwd_gqa(const void* q, const void* k, const void* v, double* o, double* lse,
+                        int B, int H, int Hkv, int M, int N, int D, double scale, int causal,
+                        int dtype) {
+  if (check_sizes(B, H, Hkv, M, N, D, dtype)) return -1;
   const int64_t rows = (int64_t)B * H * M;
   int status = 0;
 #pragma omp parallel
@@ -112,7 +123,8 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, doub
 #pragma omp for schedule(dynamic, 16)
       for (int64_t r = 0; r < rows; ++r) {
         int64_t bh = r / M, i = r % M;
-        int rc = attn_row(q, k, v, dtype, bh, i, M, N, D, scale, causal, o + r * D, lse + r, w);
+        int rc = attn_row(q, k, v, dtype, bh, kv_head(bh, H, Hkv), i, M, N, D, scale, causal,
+                          o + r * D, lse + r, w);
         if (rc) {
 #pragma omp atomic write
           status = rc;
@@ -126,11 +138,11 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, doub
 
 /* Only the listed rows; rows[t] is the flat row index (b*H + h)*M + i.
  * o is [nrows, D], lse is [nrows]. */
-int oracle_attn_fwd_rows(const void* q, const void* k, const void* v,
-                         const int64_t* rows, int64_t nrows, double* o, double* lse,
-                         int B, int H, int M, int N, int D, double scale, int causal,
-                         int dtype) {
-  if (check_sizes(B, H, M, N, D, dtype)) return -1;
+int oracle_attn_fwd_gqa_rows(const void* q, const void* k, const void* v,
+                             const int64_t* rows, int64_t nrows, double* o, double* lse,
+                             int B, int H, int Hkv, int M, int N, int D, double scale,
+                             int causal, int dtype) {
+  if (check_sizes(B, H, Hkv, M, N, D, dtype)) return -1;
   const int64_t total = (int64_t)B * H * M;
   for (int64_t t = 0; t < nrows; ++t)
     if (rows[t] < 0 || rows[t] >= total) return -1;
@@ -145,8 +157,8 @@ int oracle_attn_fwd_rows(const void* q, const void* k, const void* v,
 #pragma omp for schedule(dynamic, 4)
       for (int64_t t = 0; t < nrows; ++t) {
         int64_t r = rows[t];
-        int rc = attn_row(q, k, v, dtype, r / M, r % M, M, N, D, scale, causal,
-                          o + t * D, lse + t, w);
+        int rc = attn_row(q, k, v, dtype, r / M, kv_head(r / M, H, Hkv), r % M, M, N, D, scale,
+                          causal, o + t * D, lse + t, w);
         if (rc) {
 #pragma omp atomic write
           status = rc;
@@ -168,7 +180,7 @@ int oracle_attn_fwd_rows(const void* q, const void* k, const void* v,
 int oracle_attn_fwd_tiled(const void* q, const void* k, const void* v, double* o, double* lse,
                           int B, int H, int M, int N, int D, double scale, int causal,
                           int dtype, int BM, int BN) {
-  if (check_sizes(B, H, M, N, D, dtype) || BM <= 0 || BN <= 0) return -1;
+  if (check_sizes(B, H, H, M, N, D, dtype) || BM <= 0 || BN <= 0) return -1;
   const int64_t n_qtiles = (M + BM - 1) / BM;
   const int64_t units = (int64_t)B * H * n_qtiles;
   int status = 0;
@@ -248,4 +260,18 @@ int oracle_attn_fwd_tiled(const void* q, const void* k, const void* v, double* o
     free(s);
   }
   return status;
+}
+
+/* Multi-head attention: the Hkv == H case of the entry points above. */
+int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, double* lse,
+                    int B, int H, int M, int N, int D, double scale, int causal, int dtype) {
+  return oracle_attn_fwd_gqa(q, k, v, o, lse, B, H, H, M, N, D, scale, causal, dtype);
+}
+
+int oracle_attn_fwd_rows(const void* q, const void* k, const void* v,
+                         const int64_t* rows, int64_t nrows, double* o, double* lse,
+                         int B, int H, int M, int N, int D, double scale, int causal,
+                         int dtype) {
+  return oracle_attn_fwd_gqa_rows(q, k, v, rows, nrows, o, lse, B, H, H, M, N, D, scale,
+                                  causal, dtype);
 }

@@ -190,10 +190,33 @@ def tiled_errors(lib):
     return errs
 
 
+def gqa_errors(lib):
+    """Grouped-query attention equals multi-head attention on K/V heads repeated
+    H/Hkv times (numpy brute force), for MQA, GQA and MHA groupings."""
+    errs = []
+    for n, (B, H, Hkv, M, N, D) in enumerate([(2, 4, 1, 9, 13, 8), (3, 6, 2, 17, 5, 4),
+                                              (1, 8, 4, 12, 20, 16), (2, 3, 3, 7, 7, 2)]):
+        for dtype in (si.FP64, si.BF16):
+            q = si.normal(70 + n, 1, (B, H, M, D), 1.0, dtype)
+            k = si.normal(70 + n, 2, (B, Hkv, N, D), 1.0, dtype)
+            v = si.normal(70 + n, 3, (B, Hkv, N, D), 1.0, dtype)
+            rk, rv = (np.repeat(t, H // Hkv, axis=1) for t in (k, v))
+            for causal in (False, True):
+                o, lse = oracle.attn_fwd_gqa(q, k, v, 0.4, causal, lib=lib)
+                ob, lb = brute_force(q, rk, rv, 0.4, causal)
+                e = max(max_err(o, ob), max_err(lse, lb))
+                rows = np.array([0, M - 1, B * H * M - 1, (B * H * M) // 2], np.int64)
+                orow, lrow = oracle.attn_fwd_gqa_rows(q, k, v, 0.4, causal, rows, lib=lib)
+                e = max(e, max_err(orow, ob.reshape(-1, D)[rows]), max_err(lrow, lb.reshape(-1)[rows]))
+                if not e <= 1e-12:
+                    errs.append(f"gqa {(B, H, Hkv, M, N, D)} {dtype} causal={causal}: {e}")
+    return errs
+
+
 def all_pin_errors(lib):
     errs = []
     for check in (golden_errors, brute_errors, large_score_errors, invariant_errors,
-                  rows_errors, tiled_errors):
+                  rows_errors, tiled_errors, gqa_errors):
         try:
             errs += check(lib)
         except Exception as exc:  # a mutant may also crash or return an error code
@@ -242,6 +265,10 @@ def test_tiled_recurrence_equals_two_pass(oracle_lib):
     assert tiled_errors(oracle_lib) == []
 
 
+def test_grouped_query_attention_matches_repeated_heads(oracle_lib):
+    assert gqa_errors(oracle_lib) == []
+
+
 def test_matches_torch_sdpa_fp64():
     torch = pytest.importorskip("torch")
     import torch.nn.functional as F
@@ -284,10 +311,14 @@ MUTANTS = [
     ("L missing max", "*lse = m + log(l);", "*lse = log(l);", 1),
     ("V always row 0", "acc += w[j] * widen(v, kvoff + j * D + d, dtype);",
      "acc += w[j] * widen(v, kvoff + d, dtype);", 1),
-    ("Q row offset dropped", "const int64_t qoff = (bh * M + i) * (int64_t)D;\n  const int64_t kvoff = bh",
-     "const int64_t qoff = (bh * M) * (int64_t)D;\n  const int64_t kvoff = bh", 1),
-    ("K/V head offset dropped", "const int64_t kvoff = bh * (int64_t)N * D;\n  const int64_t nvis",
+    ("Q row offset dropped", "const int64_t qoff = (bh * M + i) * (int64_t)D;\n  const int64_t kvoff = kvh",
+     "const int64_t qoff = (bh * M) * (int64_t)D;\n  const int64_t kvoff = kvh", 1),
+    ("K/V head offset dropped", "const int64_t kvoff = kvh * (int64_t)N * D;\n  const int64_t nvis",
      "const int64_t kvoff = 0;\n  const int64_t nvis", 1),
+    ("GQA: query head mapped modulo Hkv", "return (bh / H) * Hkv + (bh % H) / (H / Hkv);",
+     "return (bh / H) * Hkv + (bh % H) % Hkv;", 1),
+    ("GQA: batch offset of the K/V head dropped", "return (bh / H) * Hkv + (bh % H) / (H / Hkv);",
+     "return (bh % H) / (H / Hkv);", 1),
     ("tiled: O not rescaled", "acc[(int64_t)r * D + d] = alpha * acc[(int64_t)r * D + d] + pv;",
      "acc[(int64_t)r * D + d] = acc[(int64_t)r * D + d] + pv;", 1),
     ("tiled: l not rescaled", "l_run[r] = alpha * l_run[r] + rowsum;", "l_run[r] = l_run[r] + rowsum;", 1),
