@@ -35,8 +35,10 @@ WORKLOAD = "bf16_2x16x8192x8192x128_causal"
 METRIC = "FA2 fwd TFLOP/s (4BHMND, 1/2 causal) and % of GB300 dense tensor peak"
 UNIT = "TFLOP/s"
 KERNEL = "fa2_fwd_kernel"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "fa2_fwd_kernel_bf16_2x16x8192x8192x128_causal.md")
+def profile_summary(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"fa2_fwd_kernel_{workload}.md")
 L2_FLUSH_BYTES = 256 << 20
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates per GPU
 
 
 def measured_peaks():
@@ -58,12 +60,13 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def dram_traffic_per_launch():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its recorded source hash matches)."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def dram_traffic_per_launch(workload: str = WORKLOAD):
+    """DRAM bytes per launch from the committed ncu summary of ``workload``, if it
+    was taken on the current kernel source (its recorded source hash matches)."""
+    path = profile_summary(workload)
+    if not os.path.exists(path):
         return None
-    text = open(PROFILE_SUMMARY).read()
+    text = open(path).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
     if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
@@ -199,12 +202,12 @@ def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
     rng = np.random.default_rng(seed)
     total_rows = w.B * w.H * w.M
     rows = np.sort(rng.choice(total_rows, size=64, replace=False))
-    oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, rows[:8])  # warm (build, pages)
+    oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows[:8])  # warm (build, pages)
     n = 64
     while True:
         rows = np.sort(rng.choice(total_rows, size=n, replace=False))
         t0 = time.perf_counter()
-        oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, rows)
+        oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
         dt = time.perf_counter() - t0
         if dt >= seconds_target or n >= total_rows:
             break
@@ -221,7 +224,7 @@ def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    w = si.WORKLOADS[WORKLOAD]
+    w = si.WORKLOADS[args.workload]
     q, k, v = si.make_qkv(w)
     per_step = []
     for step in range(args.warmup + args.steps):
@@ -234,8 +237,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "M": w.M, "N": w.N, "D": w.D,
-                   "causal": w.causal},
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M, "N": w.N,
+                   "D": w.D, "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"per step: {per_step[-1][1]} seeded random query rows of the "
                                    f"workload (fp64, all their visible keys), ~2 s of CPU work"},
@@ -249,18 +252,19 @@ def measure_e2e(args, w, q, k, v, tq, tk, tv, o, lse, step, stream, world):
     runs the forward through the C ABI and copies O and L back to pinned host
     memory, all inside the timed region."""
     import torch
+    raw = torch.int16 if tq.dtype == torch.bfloat16 else torch.float32
     hq, hk, hv = (torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
                   for a in (q, k, v))
-    ho = torch.empty(o.shape, dtype=torch.int16).pin_memory()
+    ho = torch.empty(o.shape, dtype=raw).pin_memory()
     hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    dq, dk, dv = tq.view(torch.int16), tk.view(torch.int16), tv.view(torch.int16)
+    dq, dk, dv = tq.view(raw), tk.view(raw), tv.view(raw)
 
     def e2e_step():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
         step()
-        ho.copy_(o.view(torch.int16), non_blocking=True)
+        ho.copy_(o.view(raw), non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -286,11 +290,16 @@ def run_ours(args, rank, local, world):
     import torch
     import exact_attention_forward_fa2_gb300 as fa2
 
-    w = si.WORKLOADS[WORKLOAD]
+    w = si.WORKLOADS[args.workload]
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     q, k, v = si.make_qkv(w)
-    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
     tq, tk, tv = to_dev(q), to_dev(k), to_dev(v)
     o = torch.empty_like(tq)
     lse = torch.empty((w.B, w.H, w.M), dtype=torch.float32, device=dev)
@@ -332,19 +341,25 @@ def run_ours(args, rank, local, world):
     if rank != 0:
         return
     peak, hbm_peak, peak_kind = measured_peaks()
+    peak_kind = f"bf16 dense burst, {peak_kind}"
+    if w.dtype != si.BF16:
+        # TF32 contraction: the measured bf16 peak times the nominal dense TF32/BF16 ratio
+        peak = peak * TF32_OVER_BF16
+        peak_kind = f"tf32 = {TF32_OVER_BF16:.3f} x {peak_kind} (nominal 1.1/2.25 PFLOP/s)"
     achieved = w.flops / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": w.B, "H": w.H, "M": w.M, "N": w.N, "D": w.D,
-                   "causal": w.causal, "scale": w.scale,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == si.BF16 else "tf32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M, "N": w.N,
+                   "D": w.D, "causal": w.causal, "scale": w.scale,
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "traffic": dram_traffic_per_launch(), "kernel": KERNEL,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": dram_traffic_per_launch(w.name), "kernel": KERNEL,
                      "algorithmic_flops_per_launch": w.flops,
                      "hbm_algorithmic_bytes_per_launch": w.io_bytes(),
                      "hbm_gbs_at_this_time": w.io_bytes() / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e9,
@@ -369,6 +384,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(si.WORKLOADS), default=WORKLOAD,
+                    help="workload to measure (default: the headline bf16 D=128 causal one)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")

@@ -35,6 +35,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa2_gb30
 _VP, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "fa2_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP], _I),
+    "fa2_fwd_gqa": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP], _I),
     "fa2_strerror": ([_I], ctypes.c_char_p),
     "fa2_device_status": ([_I, ctypes.POINTER(_I)], _I),
     "fa2_version": ([], _I),
@@ -89,17 +90,20 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool 
             stream=None):
     """FlashAttention-2 forward on torch CUDA tensors.
 
-    q [B,H,M,D], k and v [B,H,N,D] (bf16 or fp32, contiguous, same device); o
-    [B,H,M,D] and lse [B,H,M] fp32 are allocated when not given.  ``scale``
-    defaults to 1/sqrt(D).  Launches on ``stream`` (default: torch's current
-    stream) and returns (o, lse) without synchronising.
+    q [B,H,M,D], k and v [B,H_kv,N,D] (bf16 or fp32, contiguous, same
+    device); H_kv == H is multi-head attention, a divisor of H grouped-query
+    attention (``fa2_fwd_gqa`` in the C ABI).  o [B,H,M,D] and lse [B,H,M] fp32
+    are allocated when not given.  ``scale`` defaults to 1/sqrt(D).  Launches on
+    ``stream`` (default: torch's current stream) and returns (o, lse) without
+    synchronising.
     """
     import torch
 
-    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or q.shape[:2] != k.shape[:2] \
-            or q.shape[3] != k.shape[3]:
-        raise ValueError("expected q [B,H,M,D] and k, v [B,H,N,D]")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or q.shape[0] != k.shape[0] \
+            or q.shape[3] != k.shape[3] or k.shape[1] == 0 or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("expected q [B,H,M,D] and k, v [B,H_kv,N,D] with H_kv dividing H")
     B, H, M, D = q.shape
+    H_kv = k.shape[1]
     N = k.shape[2]
     if q.dtype == torch.bfloat16:
         dtype = FA2_BF16
@@ -125,8 +129,18 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool 
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     with torch.cuda.device(q.device):
-        rc = lib().fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                           B, H, M, N, D, float(scale), 1 if causal else 0, dtype, handle)
+        if H_kv == H:
+            rc = lib().fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, M, N, D, float(scale), 1 if causal else 0,
+                               dtype, handle)
+        else:
+            rc = lib().fa2_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, H_kv, M, N, D, float(scale),
+                                   1 if causal else 0, dtype, handle)
     if rc != FA2_OK:
         raise Fa2Error(rc, "fa2_fwd")
     return o, lse
+
+
+# The grouped-query entry has the same Python signature: k and v carry H_kv heads.
+fa2_fwd_gqa = fa2_fwd

@@ -96,11 +96,12 @@ int encode_map(CUtensorMap* map, const void* ptr, int dtype, int D, int rows, in
 
 }  // namespace
 
-extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H, int M, int N, int D, float scale, int causal, int dtype,
-                       void* stream) {
+extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int H_kv, int M, int N, int D, float scale, int causal,
+                           int dtype, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
+  if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
   if (D != 64 && D != 128) return FA2_ERR_HEADDIM;
   if (dtype != FA2_BF16 && dtype != FA2_FP32) return FA2_ERR_DTYPE;
   if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
@@ -108,6 +109,7 @@ extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, flo
   if ((addr(q) | addr(k) | addr(v) | addr(o)) & 15u) return FA2_ERR_ALIGN;
   if (addr(lse) & 3u) return FA2_ERR_ALIGN;
   const int64_t bh = static_cast<int64_t>(B) * H;
+  const int64_t bh_kv = static_cast<int64_t>(B) * H_kv;
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
   const int64_t units = bh * ((static_cast<int64_t>(M) + qt * 128 - 1) / (qt * 128));
   if (bh > INT_MAX || units > INT_MAX) return FA2_ERR_TOO_LARGE;
@@ -118,10 +120,10 @@ extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, flo
 
   fa2::FwdLaunch L;
   rc = encode_map(&L.tmQ, q, dtype, D, M, bh);
-  if (rc == FA2_OK) rc = encode_map(&L.tmK, k, dtype, D, N, bh);
+  if (rc == FA2_OK) rc = encode_map(&L.tmK, k, dtype, D, N, bh_kv);
   // fp32 V is read MN-major as TF32: 32-byte-chunk swizzle (see the kernel header)
   if (rc == FA2_OK)
-    rc = encode_map(&L.tmV, v, dtype, D, N, bh,
+    rc = encode_map(&L.tmV, v, dtype, D, N, bh_kv,
                     dtype == FA2_BF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
   if (rc == FA2_OK) rc = encode_map(&L.tmO, o, dtype, D, M, bh);
   if (rc != FA2_OK) return rc;
@@ -130,6 +132,8 @@ extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, flo
   L.params.M = M;
   L.params.N = N;
   L.params.BH = static_cast<int>(bh);
+  L.params.H = H;
+  L.params.group = H / H_kv;
   L.params.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   L.causal = causal ? 1 : 0;
   L.stream = static_cast<cudaStream_t>(stream);
@@ -142,11 +146,17 @@ extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, flo
   return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
+extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int M, int N, int D, float scale, int causal, int dtype,
+                       void* stream) {
+  return fa2_fwd_gqa(q, k, v, o, lse, B, H, H, M, N, D, scale, causal, dtype, stream);
+}
+
 extern "C" const char* fa2_strerror(int status) {
   switch (status) {
     case FA2_OK: return "ok";
     case FA2_ERR_NULL: return "a required pointer is NULL";
-    case FA2_ERR_SHAPE: return "B, H, M and N must be positive";
+    case FA2_ERR_SHAPE: return "B, H, M, N and H_kv must be positive and H_kv must divide H";
     case FA2_ERR_HEADDIM: return "head dimension D must be 64 or 128";
     case FA2_ERR_DTYPE: return "dtype must be FA2_BF16 or FA2_FP32";
     case FA2_ERR_ALIGN: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";

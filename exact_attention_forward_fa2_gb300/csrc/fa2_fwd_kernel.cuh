@@ -41,7 +41,9 @@ namespace fa2 {
 struct FwdParams {
   float* lse;           // [BH, M] fp32, written for rows < M
   int* status;          // sticky device status word (0 = ok)
-  int M, N, BH;
+  int M, N, BH;         // BH = B * H query heads
+  int H;                // query heads per batch entry
+  int group;            // query heads per key/value head (H / H_kv)
   int num_units;        // BH * ceil(M / (kQTiles * 128))
   int units_per_head;   // ceil(M / (kQTiles * 128))
   float scale_log2;     // softmax scale * log2(e)
@@ -195,6 +197,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
   const Unit unit = unit_of_block(p, kCausal);
   const int bh = unit.bh;
+  // key/value head read by this query head (grouped-query attention, "From
+  // FlashAttention to FlashAttention 2", Layer 8: h_kv = h / (H / H_kv))
+  const int bh_kv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
   int row0[C::kQTiles], nkv[C::kQTiles];
   int n_max = 0;
 #pragma unroll
@@ -264,7 +269,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffK + s * C::kTileBytes + cb * C::kBlockBytes, &tmK,
-                           bar(C::kBarKFull + s), cb * C::kSwElems, j * C::BN, bh, pol_kv);
+                           bar(C::kBarKFull + s), cb * C::kSwElems, j * C::BN, bh_kv, pol_kv);
         if (use > 0 && !wait_bounded(bar(C::kBarVEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaV)) {
           issued = -(j + 1);  // K_j issued, V_j not
           break;
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffV + s * C::kTileBytes + cb * C::kBlockBytes, &tmV,
-                           bar(C::kBarVFull + s), cb * C::kSwElems, j * C::BN, bh, pol_kv);
+                           bar(C::kBarVFull + s), cb * C::kSwElems, j * C::BN, bh_kv, pol_kv);
         issued = j + 1;
       }
       if (*wctx.abort_flag) {

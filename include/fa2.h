@@ -44,7 +44,7 @@ extern "C" {
 /* Status codes. */
 #define FA2_OK 0
 #define FA2_ERR_NULL (-1)           /* a required pointer is NULL */
-#define FA2_ERR_SHAPE (-2)          /* B, H, M or N <= 0 */
+#define FA2_ERR_SHAPE (-2)          /* B, H, M or N <= 0, or H_kv <= 0 or not dividing H */
 #define FA2_ERR_HEADDIM (-3)        /* D is not 64 or 128 */
 #define FA2_ERR_DTYPE (-4)          /* dtype is not FA2_BF16 or FA2_FP32 */
 #define FA2_ERR_ALIGN (-5)          /* q/k/v/o not 16-byte or lse not 4-byte aligned */
@@ -73,6 +73,17 @@ extern "C" {
  */
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
             int M, int N, int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * fa2_fwd_gqa -- the same forward pass with grouped-query (or multi-query)
+ * attention: k and v hold H_kv heads, [B, H_kv, N, D], H_kv divides H, and query
+ * head h attends to key/value head h / (H / H_kv) of the same batch entry
+ * ("From FlashAttention to FlashAttention 2", Layer 8: Multi-Query / Grouped-Query
+ * Attention).  H_kv == H is fa2_fwd; H_kv == 1 is multi-query attention.  All
+ * other arguments, layouts, ownership and errors are those of fa2_fwd.
+ */
+int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int H_kv, int M, int N, int D, float scale, int causal, int dtype, void* stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);

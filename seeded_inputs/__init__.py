@@ -112,6 +112,11 @@ class Workload:
     seed: int
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
+    H_kv: int = 0  # key/value heads (grouped-query attention); 0 means H
+
+    @property
+    def Hkv(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def scale(self) -> float:
@@ -126,8 +131,8 @@ class Workload:
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes: read Q, K, V once; write O and fp32 L once."""
         e = 2 if self.dtype == BF16 else 4
-        bh = self.B * self.H
-        return bh * ((2 * self.M * self.D + 2 * self.N * self.D) * e + 4 * self.M)
+        q_o = self.B * self.H * (2 * self.M * self.D * e + 4 * self.M)
+        return q_o + self.B * self.Hkv * 2 * self.N * self.D * e
 
 
 # The five workloads the method is checked and measured on. Values are iid normal;
@@ -140,12 +145,15 @@ WORKLOADS = {
     "bf16_2x16x8192x8192x128_causal": Workload("bf16_2x16x8192x8192x128_causal", 2, 16, 8192, 8192, 128, BF16, True, 4),
     "bf16_8x32x1000x3000x128_sharp": Workload("bf16_8x32x1000x3000x128_sharp", 8, 32, 1000, 3000, 128, BF16, False, 5,
                                               sigma_qk=3.0, sigma_v=1.0),
+    # grouped-query attention: 32 query heads share 8 key/value heads
+    "bf16_2x32x8192x8192x128_gqa8_causal": Workload("bf16_2x32x8192x8192x128_gqa8_causal", 2, 32, 8192, 8192, 128,
+                                                    BF16, True, 6, H_kv=8),
 }
 
 
 def make_qkv(w: Workload):
     """Draw (q, k, v) host arrays for workload ``w`` in its storage dtype."""
     q = normal(w.seed, 1, (w.B, w.H, w.M, w.D), w.sigma_qk, w.dtype)
-    k = normal(w.seed, 2, (w.B, w.H, w.N, w.D), w.sigma_qk, w.dtype)
-    v = normal(w.seed, 3, (w.B, w.H, w.N, w.D), w.sigma_v, w.dtype)
+    k = normal(w.seed, 2, (w.B, w.Hkv, w.N, w.D), w.sigma_qk, w.dtype)
+    v = normal(w.seed, 3, (w.B, w.Hkv, w.N, w.D), w.sigma_v, w.dtype)
     return q, k, v

@@ -31,7 +31,8 @@ def lib():
 
 
 def test_header_declares_the_api():
-    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_strerror", "fa2_version"]
+    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_fwd_gqa", "fa2_strerror",
+                                    "fa2_version"]
 
 
 def test_exports_every_declared_symbol(lib):
@@ -80,6 +81,24 @@ def call(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, M=8, N=8, D=64, scale=0.125, 
 ])
 def test_rejects_bad_arguments(lib, kw, code):
     assert call(lib, **kw) == code
+
+
+def call_gqa(lib, H=8, H_kv=2, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, M=8, N=8, D=64, scale=0.125, causal=0, dtype=0)
+    a.update(kw)
+    return lib.fa2_fwd_gqa(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], H, H_kv, a["M"], a["N"],
+                           a["D"], a["scale"], a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 0), (8, -1), (8, 3), (4, 8)])
+def test_gqa_rejects_bad_head_grouping(lib, H, H_kv):
+    assert call_gqa(lib, H=H, H_kv=H_kv) == fa2.FA2_ERR_SHAPE
+
+
+def test_gqa_validates_like_fa2_fwd(lib):
+    assert call_gqa(lib, q=None) == fa2.FA2_ERR_NULL
+    assert call_gqa(lib, D=96) == fa2.FA2_ERR_HEADDIM
+    assert call_gqa(lib, k=P + 4) == fa2.FA2_ERR_ALIGN
 
 
 def test_no_gpu_means_an_error_not_a_fallback(lib):

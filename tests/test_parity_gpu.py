@@ -154,16 +154,41 @@ def test_deterministic_and_stream(fa2):
     assert torch.equal(l1, l2)
 
 
+GQA = [  # (B, H, H_kv, M, N, D)
+    (2, 8, 1, 300, 517, 128),   # multi-query
+    (1, 8, 2, 256, 256, 64),
+    (2, 6, 3, 129, 1000, 128),
+    (1, 4, 4, 200, 96, 64),     # H_kv == H through the grouped entry
+]
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", GQA, ids=lambda s: "x".join(map(str, s)))
+def test_grouped_query_all_rows(fa2, shape, causal, dtype):
+    B, H, Hkv, M, N, D = shape
+    seed = 2000 + sum(shape)
+    q = si.normal(seed, 1, (B, H, M, D), 1.0, dtype)
+    k = si.normal(seed, 2, (B, Hkv, N, D), 1.0, dtype)
+    v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    o, lse = fa2.fa2_fwd_gqa(tq, tk, tv, scale=D ** -0.5, causal=causal)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, D ** -0.5, causal)
+    eo, el, excess = compare(to_host_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, l_ref, dtype)
+    assert excess <= 0 and el <= TOL[dtype], (eo, el)
+
+
 def full_or_sampled(fa2, name, sampled):
     w = si.WORKLOADS[name]
     q, k, v = si.make_qkv(w)
     o, lse = run_gpu(fa2, q, k, v, w.scale, w.causal)
     if sampled:
         rows = sample_rows(w.B, w.H, w.M, w.N, w.causal)
-        o_ref, l_ref = oracle.attn_fwd_rows(q, k, v, w.scale, w.causal, rows)
+        o_ref, l_ref = oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
         o_cmp, l_cmp = o.reshape(-1, w.D)[rows], lse.reshape(-1)[rows]
     else:
-        o_ref, l_ref = oracle.attn_fwd(q, k, v, w.scale, w.causal)
+        o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, w.scale, w.causal)
         o_cmp, l_cmp = o, lse
         # every row was written: nothing left at a sentinel, all finite
     eo, el, excess = compare(o_cmp, l_cmp, o_ref, l_ref, w.dtype)
@@ -178,6 +203,7 @@ def test_workload_full(fa2, name):
     full_or_sampled(fa2, name, sampled=False)
 
 
-@pytest.mark.parametrize("name", ["bf16_2x16x8192x8192x128", "bf16_2x16x8192x8192x128_causal"])
+@pytest.mark.parametrize("name", ["bf16_2x16x8192x8192x128", "bf16_2x16x8192x8192x128_causal",
+                                  "bf16_2x32x8192x8192x128_gqa8_causal"])
 def test_workload_sampled_rows(fa2, name):
     full_or_sampled(fa2, name, sampled=True)
