@@ -306,8 +306,20 @@ def run_ours(args, rank, local, world):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        fa2.fa2_fwd(tq, tk, tv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+    launches_per_step = 1
+    if w.split_kv:
+        dcode = fa2.FA2_BF16 if w.dtype == si.BF16 else fa2.FA2_FP32
+        n_split = fa2.fa2_splitkv_num_splits(w.B, w.H, w.M, w.N, w.D, dcode)
+        ws = torch.empty(max(256, fa2.fa2_splitkv_workspace_bytes(w.B, w.H, w.M, w.D, n_split)),
+                         dtype=torch.uint8, device=dev)
+        launches_per_step = 2 if n_split > 1 else 1  # forward slices + combine
+
+        def step():
+            fa2.fa2_fwd_splitkv(tq, tk, tv, o=o, lse=lse, scale=w.scale, causal=w.causal,
+                                num_splits=n_split, workspace=ws, stream=stream)
+    else:
+        def step():
+            fa2.fa2_fwd(tq, tk, tv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -355,7 +367,8 @@ def run_ours(args, rank, local, world):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M, "N": w.N,
                    "D": w.D, "causal": w.causal, "scale": w.scale,
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"num_splits": n_split} if w.split_kv else {})},
         "frac_of_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
@@ -365,7 +378,7 @@ def run_ours(args, rank, local, world):
                      "hbm_gbs_at_this_time": w.io_bytes() / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e9,
                      "hbm_peak_gbs": hbm_peak},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "device_status": status,
         "wall_s_timed_region": wall,

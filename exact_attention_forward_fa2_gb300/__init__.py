@@ -28,14 +28,19 @@ FA2_ERR_TOO_LARGE = -7
 FA2_ERR_ARCH = -8
 FA2_ERR_CUDA = -9
 FA2_ERR_DEVICE_TIMEOUT = -10
+FA2_ERR_WORKSPACE = -11
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa2_gb300.so")
 
 # Every symbol include/fa2.h declares, with its ctypes signature.
-_VP, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "fa2_fwd": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, _I, _I, _VP], _I),
     "fa2_fwd_gqa": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP], _I),
+    "fa2_fwd_splitkv": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP, _SZ,
+                         _VP], _I),
+    "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I], _I),
+    "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "fa2_strerror": ([_I], ctypes.c_char_p),
     "fa2_device_status": ([_I, ctypes.POINTER(_I)], _I),
     "fa2_version": ([], _I),
@@ -84,6 +89,88 @@ def fa2_device_status(reset: bool = True) -> int:
     if rc not in (FA2_OK, FA2_ERR_DEVICE_TIMEOUT):
         raise Fa2Error(rc, "fa2_device_status")
     return raw.value
+
+
+def _check_qkv(q, k, v):
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or q.shape[0] != k.shape[0] \
+            or q.shape[3] != k.shape[3] or k.shape[1] == 0 or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("expected q [B,H,M,D] and k, v [B,H_kv,N,D] with H_kv dividing H")
+    if q.dtype == torch.bfloat16:
+        dtype = FA2_BF16
+    elif q.dtype == torch.float32:
+        dtype = FA2_FP32
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    for t in (q, k, v):
+        if t.dtype != q.dtype or t.device != q.device or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one dtype and device")
+    return dtype
+
+
+def _outputs(q, o, lse):
+    import torch
+    B, H, M, _ = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    if o.shape != q.shape or o.dtype != q.dtype or not o.is_contiguous() or o.device != q.device:
+        raise ValueError("o must be a contiguous tensor like q")
+    if lse.shape != (B, H, M) or lse.dtype != torch.float32 or not lse.is_contiguous() \
+            or lse.device != q.device:
+        raise ValueError("lse must be a contiguous fp32 tensor of shape [B,H,M]")
+    return o, lse
+
+
+def _stream_handle(q, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fa2_splitkv_num_splits(B: int, H: int, M: int, N: int, D: int, dtype: int) -> int:
+    """Split count chosen by the library for the current device."""
+    rc = lib().fa2_splitkv_num_splits(B, H, M, N, D, dtype)
+    if rc < 0:
+        raise Fa2Error(rc, "fa2_splitkv_num_splits")
+    return rc
+
+
+def fa2_splitkv_workspace_bytes(B: int, H: int, M: int, D: int, num_splits: int) -> int:
+    return lib().fa2_splitkv_workspace_bytes(B, H, M, D, num_splits)
+
+
+def fa2_fwd_splitkv(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,
+                    num_splits: int = 0, workspace=None, stream=None):
+    """Split-KV forward (same result as fa2_fwd): the key range is cut into
+    ``num_splits`` slices (0 = the library's choice) whose partial results are
+    merged by a combine kernel.  ``workspace`` (a CUDA uint8 tensor) is allocated
+    with torch when not given."""
+    import torch
+
+    dtype = _check_qkv(q, k, v)
+    B, H, M, D = q.shape
+    H_kv, N = k.shape[1], k.shape[2]
+    o, lse = _outputs(q, o, lse)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        if num_splits <= 0:
+            num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype)
+        need = fa2_splitkv_workspace_bytes(B, H, M, D, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = lib().fa2_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, H_kv, M, N, D, float(scale),
+                                   1 if causal else 0, dtype, num_splits, ws_ptr, ws_len,
+                                   _stream_handle(q, stream))
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_fwd_splitkv")
+    return o, lse
 
 
 def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -17,6 +18,9 @@ cudaError_t launch_bf16_d64(FwdLaunch& L);
 cudaError_t launch_bf16_d128(FwdLaunch& L);
 cudaError_t launch_fp32_d64(FwdLaunch& L);
 cudaError_t launch_fp32_d128(FwdLaunch& L);
+cudaError_t launch_splitkv_combine(const float* o_part, const float* l_part, void* o, float* lse,
+                                   int64_t rows, int D, int num_splits, bool bf16,
+                                   cudaStream_t stream);
 }  // namespace fa2
 
 // Sticky device status word; kernels receive its address and record the first
@@ -94,11 +98,34 @@ int encode_map(CUtensorMap* map, const void* ptr, int dtype, int D, int rows, in
   return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
 }
 
-}  // namespace
+constexpr int kMaxSplits = 64;
 
-extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
-                           int B, int H, int H_kv, int M, int N, int D, float scale, int causal,
-                           int dtype, void* stream) {
+int64_t kv_tiles_total(int N) { return (static_cast<int64_t>(N) + 127) / 128; }
+
+// Split count that fills about one wave of CTAs when the query tiles alone do
+// not: floor(#SMs / units), with at least 4 key tiles per split.
+int auto_splits(int64_t units, int N, int sms) {
+  if (units >= sms) return 1;
+  int64_t s = sms / units;
+  s = std::min<int64_t>(s, kv_tiles_total(N) / 4);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits)));
+}
+
+// Byte offset of the L partials inside the workspace (after the O partials).
+size_t lpart_offset(int64_t rows, int D, int splits) {
+  const size_t o_bytes = static_cast<size_t>(splits) * static_cast<size_t>(rows) * D * sizeof(float);
+  return (o_bytes + 255) & ~static_cast<size_t>(255);
+}
+
+size_t workspace_bytes(int64_t rows, int D, int splits) {
+  return lpart_offset(rows, D, splits) + static_cast<size_t>(splits) * rows * sizeof(float);
+}
+
+// Shared by every entry point.  num_splits == 1: plain forward; > 1: split-KV
+// partials into `workspace`, then the combine kernel.
+int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int H_kv, int M, int N, int D, float scale, int causal, int dtype, int num_splits,
+                void* workspace, size_t workspace_size, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
   if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
@@ -113,6 +140,20 @@ extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o,
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
   const int64_t units = bh * ((static_cast<int64_t>(M) + qt * 128 - 1) / (qt * 128));
   if (bh > INT_MAX || units > INT_MAX) return FA2_ERR_TOO_LARGE;
+  const int64_t n_kv = kv_tiles_total(N);
+  int tiles_per_split = static_cast<int>(n_kv);
+  if (num_splits > 1) {
+    tiles_per_split = static_cast<int>((n_kv + num_splits - 1) / num_splits);
+    num_splits = static_cast<int>((n_kv + tiles_per_split - 1) / tiles_per_split);
+  }
+  if (num_splits < 1) num_splits = 1;
+  if (units * num_splits > INT_MAX) return FA2_ERR_TOO_LARGE;
+  const int64_t rows = bh * M;
+  if (num_splits > 1) {
+    const auto wa = reinterpret_cast<uintptr_t>(workspace);
+    if (!workspace || (wa & 255u) || workspace_size < workspace_bytes(rows, D, num_splits))
+      return FA2_ERR_WORKSPACE;
+  }
 
   DeviceState* st = nullptr;
   int rc = device_state(&st);
@@ -134,6 +175,13 @@ extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o,
   L.params.BH = static_cast<int>(bh);
   L.params.H = H;
   L.params.group = H / H_kv;
+  L.params.num_splits = num_splits;
+  L.params.tiles_per_split = tiles_per_split;
+  L.params.o_part = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  L.params.l_part = num_splits > 1
+                        ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                   lpart_offset(rows, D, num_splits))
+                        : nullptr;
   L.params.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   L.causal = causal ? 1 : 0;
   L.stream = static_cast<cudaStream_t>(stream);
@@ -143,7 +191,58 @@ extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o,
     e = (D == 64) ? fa2::launch_bf16_d64(L) : fa2::launch_bf16_d128(L);
   else
     e = (D == 64) ? fa2::launch_fp32_d64(L) : fa2::launch_fp32_d128(L);
+  if (e == cudaSuccess && num_splits > 1)
+    e = fa2::launch_splitkv_combine(L.params.o_part, L.params.l_part, o, lse, rows, D, num_splits,
+                                    dtype == FA2_BF16, L.stream);
   return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+int sm_count(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return FA2_ERR_CUDA;
+  return FA2_OK;
+}
+
+}  // namespace
+
+extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int H_kv, int M, int N, int D, float scale, int causal,
+                           int dtype, void* stream) {
+  return run_forward(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, causal, dtype, 1, nullptr, 0,
+                     stream);
+}
+
+extern "C" int fa2_splitkv_num_splits(int B, int H, int M, int N, int D, int dtype) {
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
+  if (D != 64 && D != 128) return FA2_ERR_HEADDIM;
+  if (dtype != FA2_BF16 && dtype != FA2_FP32) return FA2_ERR_DTYPE;
+  int sms = 0;
+  const int rc = sm_count(&sms);
+  if (rc != FA2_OK) return rc;
+  const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
+  const int64_t units =
+      static_cast<int64_t>(B) * H * ((static_cast<int64_t>(M) + qt * 128 - 1) / (qt * 128));
+  return auto_splits(units, N, sms);
+}
+
+extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits) {
+  if (B <= 0 || H <= 0 || M <= 0 || (D != 64 && D != 128) || num_splits <= 1) return 0;
+  return workspace_bytes(static_cast<int64_t>(B) * H * M, D, num_splits);
+}
+
+extern "C" int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int H_kv, int M, int N, int D, float scale,
+                               int causal, int dtype, int num_splits, void* workspace,
+                               size_t workspace_size, void* stream) {
+  if (num_splits <= 0) {
+    num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype);
+    if (num_splits < 0) return num_splits;
+  }
+  if (num_splits > kMaxSplits) num_splits = kMaxSplits;
+  return run_forward(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, causal, dtype, num_splits,
+                     workspace, workspace_size, stream);
 }
 
 extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -165,6 +264,7 @@ extern "C" const char* fa2_strerror(int status) {
     case FA2_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103)";
     case FA2_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case FA2_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait ran out of time";
+    case FA2_ERR_WORKSPACE: return "split-KV workspace missing, not 256-byte aligned or too small";
     default: return "unknown status";
   }
 }

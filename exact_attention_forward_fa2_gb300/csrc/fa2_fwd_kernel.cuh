@@ -47,6 +47,13 @@ struct FwdParams {
   int num_units;        // BH * ceil(M / (kQTiles * 128))
   int units_per_head;   // ceil(M / (kQTiles * 128))
   float scale_log2;     // softmax scale * log2(e)
+  // split-KV: the key range is cut into num_splits slices of tiles_per_split key
+  // tiles; with more than one slice each CTA writes a partial (O_s = its P V / l_s
+  // in fp32, L_s = m_s + ln l_s) instead of O and L, merged by the combine kernel
+  int num_splits;
+  int tiles_per_split;
+  float* o_part;        // [num_splits][BH][M][D] fp32 (num_splits > 1)
+  float* l_part;        // [num_splits][BH][M] fp32 (num_splits > 1)
 };
 
 // Device status codes (first failing wait site wins).
@@ -125,9 +132,8 @@ struct Unit {
 // Causal units are launched longest first (largest query offset, heads
 // interleaved) so the tail of the grid holds the short ones; non-causal units
 // keep one head's query tiles adjacent so its K/V stay hot in L2.
-__device__ __forceinline__ Unit unit_of_block(const FwdParams& p, bool causal) {
+__device__ __forceinline__ Unit unit_of_block(const FwdParams& p, bool causal, int b) {
   Unit u;
-  const int b = static_cast<int>(blockIdx.x);
   if (causal) {
     u.pair = p.units_per_head - 1 - b / p.BH;
     u.bh = b % p.BH;
@@ -145,6 +151,14 @@ __device__ __forceinline__ int kv_tiles_for(int row0, int M, int N, bool causal)
   if (!causal) return total;
   const int last_row = min(row0 + 128, M) - 1;
   return min(total, last_row / 128 + 1);
+}
+
+// Key tiles of that query tile inside split `split` (tiles [split*tps, +tps)):
+// the count; the first one is split*tps.
+__device__ __forceinline__ int kv_tiles_in_split(int row0, const FwdParams& p, bool causal,
+                                                 int split) {
+  const int n = kv_tiles_for(row0, p.M, p.N, causal) - split * p.tiles_per_split;
+  return max(0, min(n, p.tiles_per_split));
 }
 
 struct WaitCtx {
@@ -195,7 +209,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   const int lane = static_cast<int>(threadIdx.x) % 32;
   auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
 
-  const Unit unit = unit_of_block(p, kCausal);
+  const int split = static_cast<int>(blockIdx.x) % p.num_splits;
+  const int kb = split * p.tiles_per_split;  // first key tile of this CTA's split
+  const Unit unit = unit_of_block(p, kCausal, static_cast<int>(blockIdx.x) / p.num_splits);
   const int bh = unit.bh;
   // key/value head read by this query head (grouped-query attention, "From
   // FlashAttention to FlashAttention 2", Layer 8: h_kv = h / (H / H_kv))
@@ -205,7 +221,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
   for (int t = 0; t < C::kQTiles; ++t) {
     row0[t] = (unit.pair * C::kQTiles + t) * C::BM;
-    nkv[t] = kv_tiles_for(row0[t], p.M, p.N, kCausal);
+    nkv[t] = kv_tiles_in_split(row0[t], p, kCausal, split);
     n_max = max(n_max, nkv[t]);
   }
 
@@ -269,7 +285,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffK + s * C::kTileBytes + cb * C::kBlockBytes, &tmK,
-                           bar(C::kBarKFull + s), cb * C::kSwElems, j * C::BN, bh_kv, pol_kv);
+                           bar(C::kBarKFull + s), cb * C::kSwElems, (kb + j) * C::BN, bh_kv, pol_kv);
         if (use > 0 && !wait_bounded(bar(C::kBarVEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaV)) {
           issued = -(j + 1);  // K_j issued, V_j not
           break;
@@ -278,7 +294,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffV + s * C::kTileBytes + cb * C::kBlockBytes, &tmV,
-                           bar(C::kBarVFull + s), cb * C::kSwElems, j * C::BN, bh_kv, pol_kv);
+                           bar(C::kBarVFull + s), cb * C::kSwElems, (kb + j) * C::BN, bh_kv, pol_kv);
         issued = j + 1;
       }
       if (*wctx.abort_flag) {
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
     const int tile_row0 = (unit.pair * C::kQTiles + t) * C::BM;
     const int row = tile_row0 + r;
-    const int n_t = kv_tiles_for(tile_row0, p.M, p.N, kCausal);
+    const int n_t = kv_tiles_in_split(tile_row0, p, kCausal, split);
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS(t);
     const uint32_t tO = tmem + lane_addr + C::kColO(t);
@@ -396,7 +412,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
       // mask keys past N and, when causal, keys after this row (boundary tiles only)
-      const int key0 = j * C::BN;
+      const int key0 = (kb + j) * C::BN;
       const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
       if (boundary) {
         int lim = p.N - 1 - key0;
@@ -489,7 +505,42 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    if (n_t > 0) {
+    if (p.num_splits > 1) {
+      // split-KV partial for the rows of this tile: O_s = O/l_s in fp32, L_s (natural
+      // log); a split without visible keys for the tile contributes O_s = 0, L_s = -inf
+      if (tile_row0 < p.M) {
+        if (n_t > 0 && ok)
+          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
+                                                    kStatusTimeoutEpilogue));
+        const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh) * p.M + row;
+        float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D);
+        if (n_t > 0 && ok) {
+          tc_fence_after_sync();
+          const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+#pragma unroll
+          for (int ch = 0; ch < C::D / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld_x32(tO + ch * 32, v);
+            tmem_ld_wait();
+            reg_fence_x32(v);
+            if (row < p.M) {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                op[ch * 8 + q4] = make_float4(__uint_as_float(v[q4 * 4 + 0]) * inv_l,
+                                              __uint_as_float(v[q4 * 4 + 1]) * inv_l,
+                                              __uint_as_float(v[q4 * 4 + 2]) * inv_l,
+                                              __uint_as_float(v[q4 * 4 + 3]) * inv_l);
+            }
+          }
+          if (row < p.M)
+            p.l_part[prow] = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
+        } else if (n_t == 0 && row < p.M) {
+#pragma unroll
+          for (int q4 = 0; q4 < C::D / 4; ++q4) op[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.l_part[prow] = -INFINITY;
+        }
+      }
+    } else if (n_t > 0) {
       if (ok)
         ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
                                                   kStatusTimeoutEpilogue));

@@ -26,7 +26,7 @@ cudaError_t launch_cfg(FwdLaunch& L) {
   }
   L.params.units_per_head = (L.params.M + C::kQTiles * C::BM - 1) / (C::kQTiles * C::BM);
   L.params.num_units = L.params.units_per_head * L.params.BH;
-  const dim3 grid(static_cast<unsigned>(L.params.num_units));
+  const dim3 grid(static_cast<unsigned>(L.params.num_units * L.params.num_splits));
   const dim3 block(C::kThreads);
   if (L.causal)
     fa2_fwd_kernel<C, true><<<grid, block, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmO,

@@ -33,6 +33,8 @@
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -53,6 +55,7 @@ extern "C" {
 #define FA2_ERR_ARCH (-8)           /* current device is not compute capability 10.3 */
 #define FA2_ERR_CUDA (-9)           /* a CUDA runtime or driver call failed */
 #define FA2_ERR_DEVICE_TIMEOUT (-10) /* a kernel gave up on a pipeline wait (see fa2_device_status) */
+#define FA2_ERR_WORKSPACE (-11)     /* split-KV workspace missing, misaligned or too small */
 
 /*
  * fa2_fwd -- FlashAttention-2 forward pass.
@@ -84,6 +87,38 @@ int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
  */
 int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int H_kv, int M, int N, int D, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Split-KV forward ("From FlashAttention to FlashAttention 2", Layer 2: the
+ * split-KV dispatch when num_splits > 1).  When B*H*(query tiles) cannot fill the
+ * GPU (short M, long N), the key range is cut into num_splits slices: each slice
+ * computes a partial result over its keys (O_s normalised by its own row sum,
+ * L_s = its logsumexp) into `workspace`, and a combine kernel merges them into O
+ * and L:  L = ln sum_s exp(L_s),  O = sum_s exp(L_s - L) O_s.  The result is the
+ * same attention as fa2_fwd_gqa (up to rounding).
+ *
+ *   num_splits  number of key slices; <= 0 picks fa2_splitkv_num_splits(); it is
+ *               reduced so that no slice is empty (at most ceil(N/128) slices)
+ *               and capped at 64; 1 runs the plain forward (workspace unused)
+ *   workspace   caller-owned DEVICE buffer, 256-byte aligned, of at least
+ *               fa2_splitkv_workspace_bytes(B, H, M, D, num_splits) bytes; its
+ *               contents on entry are ignored and on return are scratch
+ * All other arguments as fa2_fwd_gqa.  Returns FA2_ERR_WORKSPACE if the workspace
+ * is needed and missing, misaligned or too small.  Two kernels are launched on
+ * `stream`; concurrent calls must not share a workspace.
+ */
+int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int H_kv, int M, int N, int D, float scale, int causal, int dtype,
+                    int num_splits, void* workspace, size_t workspace_size, void* stream);
+
+/* Split count fa2_fwd_splitkv uses when given num_splits <= 0, for the current
+ * device (about one wave of CTAs, at least 4 key tiles per slice); >= 1, or a
+ * negative FA2_ERR_* code for invalid sizes or when the device cannot be queried. */
+int fa2_splitkv_num_splits(int B, int H, int M, int N, int D, int dtype);
+
+/* Workspace bytes fa2_fwd_splitkv needs for num_splits slices (0 if num_splits <= 1
+ * or the sizes are invalid): num_splits * B*H*M * (D + 1) * 4 plus padding. */
+size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);

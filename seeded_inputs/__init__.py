@@ -113,6 +113,7 @@ class Workload:
     sigma_qk: float = 1.0
     sigma_v: float = 1.0
     H_kv: int = 0  # key/value heads (grouped-query attention); 0 means H
+    split_kv: bool = False  # measured through the split-KV entry
 
     @property
     def Hkv(self) -> int:
@@ -148,6 +149,10 @@ WORKLOADS = {
     # grouped-query attention: 32 query heads share 8 key/value heads
     "bf16_2x32x8192x8192x128_gqa8_causal": Workload("bf16_2x32x8192x8192x128_gqa8_causal", 2, 32, 8192, 8192, 128,
                                                     BF16, True, 6, H_kv=8),
+    # short queries against a long key range (a prefill chunk against a long
+    # cache): 32 query-tile units cannot fill the GPU, so the key range is split
+    "bf16_1x32x128x32768x128_gqa8_splitkv": Workload("bf16_1x32x128x32768x128_gqa8_splitkv", 1, 32, 128, 32768, 128,
+                                                     BF16, False, 7, H_kv=8, split_kv=True),
 }
 
 

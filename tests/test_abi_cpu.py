@@ -31,8 +31,9 @@ def lib():
 
 
 def test_header_declares_the_api():
-    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_fwd_gqa", "fa2_strerror",
-                                    "fa2_version"]
+    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_splitkv",
+                                    "fa2_splitkv_num_splits", "fa2_splitkv_workspace_bytes",
+                                    "fa2_strerror", "fa2_version"]
 
 
 def test_exports_every_declared_symbol(lib):
@@ -99,6 +100,35 @@ def test_gqa_validates_like_fa2_fwd(lib):
     assert call_gqa(lib, q=None) == fa2.FA2_ERR_NULL
     assert call_gqa(lib, D=96) == fa2.FA2_ERR_HEADDIM
     assert call_gqa(lib, k=P + 4) == fa2.FA2_ERR_ALIGN
+
+
+def test_splitkv_workspace_bytes(lib):
+    B, H, M, D, S = 2, 3, 100, 128, 5
+    o_bytes = S * B * H * M * D * 4
+    want = ((o_bytes + 255) // 256) * 256 + S * B * H * M * 4
+    assert lib.fa2_splitkv_workspace_bytes(B, H, M, D, S) == want
+    assert lib.fa2_splitkv_workspace_bytes(B, H, M, D, 1) == 0
+    assert lib.fa2_splitkv_workspace_bytes(B, H, M, 96, S) == 0
+
+
+def call_split(lib, num_splits=4, ws=P, ws_bytes=1 << 30, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, H=8, H_kv=2, M=8, N=4096, D=64, scale=0.125, causal=0,
+             dtype=0)
+    a.update(kw)
+    return lib.fa2_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["H_kv"],
+                               a["M"], a["N"], a["D"], a["scale"], a["causal"], a["dtype"], num_splits,
+                               ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [dict(ws=None), dict(ws=P + 16), dict(ws_bytes=1024)])
+def test_splitkv_rejects_bad_workspace(lib, kw):
+    assert call_split(lib, **kw) == fa2.FA2_ERR_WORKSPACE
+
+
+def test_splitkv_validates_like_fa2_fwd(lib):
+    assert call_split(lib, q=None) == fa2.FA2_ERR_NULL
+    assert call_split(lib, H_kv=3) == fa2.FA2_ERR_SHAPE
+    assert call_split(lib, D=32) == fa2.FA2_ERR_HEADDIM
 
 
 def test_no_gpu_means_an_error_not_a_fallback(lib):

@@ -179,10 +179,59 @@ def test_grouped_query_all_rows(fa2, shape, causal, dtype):
     assert excess <= 0 and el <= TOL[dtype], (eo, el)
 
 
+SPLIT = [  # (B, H, H_kv, M, N, D, num_splits); 0 = the library's choice
+    (1, 4, 4, 128, 4096, 128, 0),
+    (2, 8, 2, 100, 3000, 64, 3),     # ragged M and N, grouped heads
+    (1, 2, 1, 1, 2000, 128, 7),      # one query row, multi-query
+    (1, 4, 4, 300, 1000, 128, 8),    # causal: later slices lie past some tiles' diagonal
+    (1, 1, 1, 256, 130, 64, 2),      # second slice holds a 2-key tail
+]
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: "x".join(map(str, s)))
+def test_split_kv_all_rows(fa2, shape, causal, dtype):
+    B, H, Hkv, M, N, D, splits = shape
+    seed = 3000 + sum(shape)
+    q = si.normal(seed, 1, (B, H, M, D), 1.0, dtype)
+    k = si.normal(seed, 2, (B, Hkv, N, D), 1.0, dtype)
+    v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    # a workspace full of NaN: every value the combine reads must have been written
+    ns = splits if splits > 0 else fa2.fa2_splitkv_num_splits(B, H, M, N, D, 0 if dtype == si.BF16 else 1)
+    nbytes = max(256, fa2.fa2_splitkv_workspace_bytes(B, H, M, D, ns))
+    ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=DEV).view(torch.uint8)
+    o, lse = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=D ** -0.5, causal=causal, num_splits=ns, workspace=ws)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, D ** -0.5, causal)
+    eo, el, excess = compare(to_host_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, l_ref, dtype)
+    assert excess <= 0 and el <= TOL[dtype], (eo, el)
+
+
+def test_split_kv_matches_unsplit_closely(fa2):
+    """Same inputs through one slice and through several: the merge changes only
+    rounding, so the two differ far less than either differs from fp64."""
+    B, H, M, N, D = 2, 4, 256, 4096, 128
+    q, k, v = inputs(31, B, H, M, N, D, si.BF16)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    o1, l1 = fa2.fa2_fwd(tq, tk, tv)
+    o2, l2 = fa2.fa2_fwd_splitkv(tq, tk, tv, num_splits=8)
+    torch.cuda.synchronize()
+    assert float((l1 - l2).abs().max()) < 2e-3
+    assert float((o1.float() - o2.float()).abs().max()) < 1e-2
+
+
 def full_or_sampled(fa2, name, sampled):
     w = si.WORKLOADS[name]
     q, k, v = si.make_qkv(w)
-    o, lse = run_gpu(fa2, q, k, v, w.scale, w.causal)
+    if w.split_kv:
+        tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+        to, tl = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=w.scale, causal=w.causal)
+        torch.cuda.synchronize()
+        o, lse = to_host_f64(to), tl.cpu().numpy().astype(np.float64)
+    else:
+        o, lse = run_gpu(fa2, q, k, v, w.scale, w.causal)
     if sampled:
         rows = sample_rows(w.B, w.H, w.M, w.N, w.causal)
         o_ref, l_ref = oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
@@ -198,7 +247,8 @@ def full_or_sampled(fa2, name, sampled):
 
 
 @pytest.mark.parametrize("name", ["fp32_1x1x128x128x64", "tf32_4x12x2048x2048x64",
-                                  "bf16_4x16x4096x4096x64_causal", "bf16_8x32x1000x3000x128_sharp"])
+                                  "bf16_4x16x4096x4096x64_causal", "bf16_8x32x1000x3000x128_sharp",
+                                  "bf16_1x32x128x32768x128_gqa8_splitkv"])
 def test_workload_full(fa2, name):
     full_or_sampled(fa2, name, sampled=False)
 
