@@ -39,6 +39,8 @@ SIGNATURES = {
     "fa2_fwd_gqa": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP], _I),
     "fa2_fwd_splitkv": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _VP, _SZ,
                          _VP], _I),
+    "fa2_fwd_splitkv_noalloc": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I,
+                                 _VP], _I),
     "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I], _I),
     "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "fa2_strerror": ([_I], ctypes.c_char_p),

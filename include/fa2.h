@@ -120,6 +120,30 @@ int fa2_splitkv_num_splits(int B, int H, int M, int N, int D, int dtype);
  * or the sizes are invalid): num_splits * B*H*M * (D + 1) * 4 plus padding. */
 size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits);
 
+/*
+ * fa2_fwd_splitkv_noalloc -- fa2_fwd_splitkv for callers that cannot allocate
+ * device memory (an exhausted or locked-down allocator, a host framework that
+ * owns every allocation, or code that must not call cudaMalloc/cudaFree because
+ * they synchronise the device).  The split-KV partials go to a buffer built into
+ * the library: a 32 MiB array in device memory that every GPU which loads the
+ * library's device code holds until the process exits.  This call allocates
+ * nothing.  The pages have no counterpart to it; it is an interface addition.
+ *
+ * Arguments as fa2_fwd_splitkv, without the workspace.  Limit: the partials,
+ * fa2_splitkv_workspace_bytes(B, H, M, D, num_splits) bytes, must fit in the
+ * 32 MiB buffer, else FA2_ERR_WORKSPACE is returned and nothing runs (pass a
+ * smaller num_splits, or use fa2_fwd_splitkv with your own workspace).
+ * The first call on a device, with that device current, looks up the buffer's
+ * device address (and may load the library's device code); make that first call
+ * before any stream capture.  All calls on a device share the one buffer, which
+ * keeps the previous call's contents (nothing in it needs to start at zero):
+ * calls whose kernels may overlap on the GPU (different streams without
+ * ordering, or several threads) race on it and must be serialised by the caller.
+ */
+int fa2_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int H_kv, int M, int N, int D, float scale, int causal,
+                            int dtype, int num_splits, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);
 

@@ -32,8 +32,8 @@ def lib():
 
 def test_header_declares_the_api():
     assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_splitkv",
-                                    "fa2_splitkv_num_splits", "fa2_splitkv_workspace_bytes",
-                                    "fa2_strerror", "fa2_version"]
+                                    "fa2_fwd_splitkv_noalloc", "fa2_splitkv_num_splits",
+                                    "fa2_splitkv_workspace_bytes", "fa2_strerror", "fa2_version"]
 
 
 def test_exports_every_declared_symbol(lib):
