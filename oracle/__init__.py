@@ -65,6 +65,9 @@ def _bind(lib):
     lib.oracle_attn_fwd_gqa_rows.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32,
                                              i32, dbl, i32, i32]
     lib.oracle_attn_fwd_gqa_rows.restype = i32
+    lib.oracle_attn_fwd_mod.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32,
+                                        dbl, i32, i32, i32, dbl, vp, i64, i32]
+    lib.oracle_attn_fwd_mod.restype = i32
     return lib
 
 
@@ -152,4 +155,42 @@ def attn_fwd_gqa_rows(q, k, v, scale: float, causal: bool, rows, lib=None):
                                       B, H, Hkv, M, N, D, float(scale), int(causal), code)
     if rc:
         raise RuntimeError(f"oracle_attn_fwd_gqa_rows failed: {rc}")
+    return o, lse
+
+
+def attn_fwd_mod(q, k, v, scale: float, causal: bool, window=(-1, -1), softcap: float = 0.0,
+                 alibi_slopes=None, rows=None, lib=None):
+    """Attention with score modifiers (sliding window, softcap, ALiBi; see
+    ``fa2_oracle.c`` for the reading).  q [B,H,M,D], k and v [B,Hkv,N,D];
+    ``window`` = (left, right), negative = unbounded; ``alibi_slopes`` None,
+    [H] (shared by every batch entry) or [B,H].  With ``rows`` None returns
+    (O [B,H,M,D], L [B,H,M]), else (O [n,D], L [n]) for the listed flat rows."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v, gqa=True)
+    Hkv = k.shape[1]
+    slopes_ptr, sb = None, 0
+    if alibi_slopes is not None:
+        sl = np.ascontiguousarray(alibi_slopes, dtype=np.float64)
+        if sl.shape == (H,):
+            sb = 0
+        elif sl.shape == (B, H):
+            sb = H
+        else:
+            raise ValueError("alibi_slopes must be [H] or [B, H]")
+        slopes_ptr = sl.ctypes.data
+    if rows is None:
+        rows_arr, n, rows_ptr = None, B * H * M, None
+        o = np.empty((B, H, M, D), np.float64)
+        lse = np.empty((B, H, M), np.float64)
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n, rows_ptr = rows_arr.size, rows_arr.ctypes.data
+        o = np.empty((n, D), np.float64)
+        lse = np.empty((n,), np.float64)
+    wl, wr = (int(x) for x in window)
+    rc = lib.oracle_attn_fwd_mod(q.ctypes.data, k.ctypes.data, v.ctypes.data, rows_ptr, n,
+                                 o.ctypes.data, lse.ctypes.data, B, H, Hkv, M, N, D, float(scale),
+                                 int(causal), wl, wr, float(softcap), slopes_ptr, sb, code)
+    if rc:
+        raise RuntimeError(f"oracle_attn_fwd_mod failed: {rc}")
     return o, lse

@@ -262,6 +262,106 @@ int oracle_attn_fwd_tiled(const void* q, const void* k, const void* v, double* o
   return status;
 }
 
+/* ---------------------------------------------------------------------------
+ * Score modifiers: sliding window, softcap and ALiBi.  The pages name these
+ * options of the forward ("From FlashAttention to FlashAttention 2", Layer 1:
+ * Python API: window_size, softcap, alibi_slopes) and describe the window as a
+ * change of the causal mask formula and ALiBi as a bias added to the score
+ * ("Writing FlashAttention 2 in Triton", What to do after your FA2 works, items
+ * 3 and 4) without printing formulas.  The reading used, for query row i of
+ * head (b, h) and key j:
+ *   s_j = scale * q_i . k_j
+ *   softcap c > 0:   s_j <- c * tanh(s_j / c)
+ *   ALiBi slope a:   s_j <- s_j - a * |i - j|       (a = slopes[b*sb + h])
+ *   visible:  0 <= j < N;  j <= i when causal;  j >= i - wl when wl >= 0;
+ *             j <= i + wr when wr >= 0            (wl, wr < 0: unbounded)
+ * then the plain softmax over the visible keys.  A window can leave a row with
+ * no visible key ("Writing FlashAttention 2 in Triton", bug catalogue item 8);
+ * such a row gets O = 0 and L = -inf. */
+static int attn_row_mod(const void* q, const void* k, const void* v, int dtype, int64_t bh,
+                        int64_t kvh, int64_t i, int H, int M, int N, int D, double scale,
+                        int causal, int wl, int wr, double softcap, const double* slopes,
+                        int64_t slope_bstride, double* o_row, double* lse, double* w) {
+  const int64_t kvoff = kvh * (int64_t)N * D;
+  const int64_t qoff = (bh * M + i) * (int64_t)D;
+  int64_t lo = 0, hi = (int64_t)N - 1; /* visible keys: lo <= j <= hi */
+  if (causal && i < hi) hi = i;
+  if (wr >= 0 && i + wr < hi) hi = i + wr;
+  if (wl >= 0 && i - wl > lo) lo = i - wl;
+  if (lo > hi) {
+    for (int d = 0; d < D; ++d) o_row[d] = 0.0;
+    *lse = -INFINITY;
+    return 0;
+  }
+  const double slope = slopes ? slopes[(bh / H) * slope_bstride + bh % H] : 0.0;
+
+  double m = -INFINITY;
+  for (int64_t j = lo; j <= hi; ++j) {
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d)
+      dot += widen(q, qoff + d, dtype) * widen(k, kvoff + j * D + d, dtype);
+    double s = scale * dot;
+    if (softcap > 0.0) s = softcap * tanh(s / softcap);
+    s -= slope * fabs((double)(i - j));
+    w[j - lo] = s;
+    if (s > m) m = s;
+  }
+  double lsum = 0.0;
+  for (int64_t j = lo; j <= hi; ++j) {
+    w[j - lo] = exp(w[j - lo] - m);
+    lsum += w[j - lo];
+  }
+  for (int d = 0; d < D; ++d) {
+    double acc = 0.0;
+    for (int64_t j = lo; j <= hi; ++j) acc += w[j - lo] * widen(v, kvoff + j * D + d, dtype);
+    o_row[d] = acc / lsum;
+  }
+  *lse = m + log(lsum);
+  return 0;
+}
+
+/* Rows of attention with score modifiers.  rows == NULL: every row, o [B,H,M,D]
+ * and lse [B,H,M]; otherwise the nrows listed flat rows (b*H + h)*M + i, o
+ * [nrows, D] and lse [nrows].  slopes: NULL (no ALiBi) or fp64 slopes read at
+ * b*slope_bstride + h (slope_bstride 0: one slope per head for every batch
+ * entry; H: one per (b, h)). */
+int oracle_attn_fwd_mod(const void* q, const void* k, const void* v, const int64_t* rows,
+                        int64_t nrows, double* o, double* lse, int B, int H, int Hkv, int M,
+                        int N, int D, double scale, int causal, int wl, int wr, double softcap,
+                        const double* slopes, int64_t slope_bstride, int dtype) {
+  if (check_sizes(B, H, Hkv, M, N, D, dtype)) return -1;
+  if (!(softcap >= 0.0) || isinf(softcap)) return -1;
+  if (slopes && slope_bstride != 0 && slope_bstride != H) return -1;
+  const int64_t total = (int64_t)B * H * M;
+  if (rows == NULL) nrows = total;
+  for (int64_t t = 0; rows && t < nrows; ++t)
+    if (rows[t] < 0 || rows[t] >= total) return -1;
+  int status = 0;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!w) {
+#pragma omp atomic write
+      status = -2;
+    } else {
+#pragma omp for schedule(dynamic, 8)
+      for (int64_t t = 0; t < nrows; ++t) {
+        const int64_t r = rows ? rows[t] : t;
+        const int64_t bh = r / M;
+        int rc = attn_row_mod(q, k, v, dtype, bh, kv_head(bh, H, Hkv), r % M, H, M, N, D, scale,
+                              causal, wl, wr, softcap, slopes, slope_bstride, o + t * D, lse + t,
+                              w);
+        if (rc) {
+#pragma omp atomic write
+          status = rc;
+        }
+      }
+      free(w);
+    }
+  }
+  return status;
+}
+
 /* Multi-head attention: the Hkv == H case of the entry points above. */
 int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, double* lse,
                     int B, int H, int M, int N, int D, double scale, int causal, int dtype) {

@@ -213,10 +213,168 @@ def gqa_errors(lib):
     return errs
 
 
+def brute_force_mod(q, k, v, scale, causal, window=(-1, -1), softcap=0.0, slopes=None):
+    """Materialise S with the score modifiers, mask, logsumexp (fp64); rows
+    without a visible key get O = 0 and L = -inf.  k, v may hold fewer heads
+    (grouped-query attention): they are repeated to H heads."""
+    q, k, v = widen(q), widen(k), widen(v)
+    B, H, M, _ = q.shape
+    N = k.shape[2]
+    k, v = (np.repeat(t, H // t.shape[1], axis=1) for t in (k, v))
+    s = scale * np.matmul(q, np.swapaxes(k, -1, -2))
+    if softcap > 0:
+        s = softcap * np.tanh(s / softcap)
+    i, j = np.arange(M)[:, None], np.arange(N)[None, :]
+    if slopes is not None:
+        a = np.broadcast_to(np.asarray(slopes, np.float64).reshape(-1, H), (B, H))
+        s = s - a[:, :, None, None] * np.abs(i - j)[None, None]
+    vis = np.ones((M, N), bool)
+    if causal:
+        vis &= j <= i
+    if window[0] >= 0:
+        vis &= j >= i - window[0]
+    if window[1] >= 0:
+        vis &= j <= i + window[1]
+    s = np.where(vis, s, -np.inf)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        lse = scipy.special.logsumexp(s, axis=-1)
+        p = np.where(vis, np.exp(s - lse[..., None]), 0.0)
+    return np.matmul(p, v), lse
+
+
+def same(a, b, tol):
+    """Elementwise |a - b| <= tol, with equal infinities counted as equal."""
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    inf = np.isinf(a) | np.isinf(b)
+    return bool(np.all(a[inf] == b[inf]) and np.all(np.abs(a[~inf] - b[~inf]) <= tol))
+
+
+MOD_CASES = [  # (B, H, Hkv, M, N, D, causal, window, softcap, slopes shape)
+    (1, 2, 2, 17, 23, 8, False, (-1, -1), 0.0, None),
+    (2, 2, 1, 19, 19, 4, True, (-1, -1), 0.0, None),
+    (1, 3, 3, 21, 13, 8, False, (4, 2), 0.0, None),
+    (2, 2, 2, 30, 9, 2, False, (3, -1), 0.0, None),   # rows past N + 3 see no key
+    (1, 2, 1, 16, 27, 8, True, (5, -1), 0.0, None),
+    (1, 2, 2, 11, 40, 4, False, (-1, 6), 0.0, None),
+    (2, 1, 1, 12, 12, 16, False, (-1, -1), 2.5, None),
+    (1, 4, 2, 13, 17, 8, True, (-1, -1), 0.0, "h"),
+    (2, 3, 3, 15, 20, 4, False, (-1, -1), 0.0, "bh"),
+    (2, 2, 2, 25, 18, 8, True, (6, 0), 1.5, "bh"),
+    (1, 2, 2, 9, 30, 8, False, (2, 3), 4.0, "h"),
+]
+
+
+def mod_brute_errors(lib):
+    """Score modifiers against the numpy brute force, every row and the row
+    entry, bf16 and fp64 inputs."""
+    errs = []
+    for n, (B, H, Hkv, M, N, D, causal, window, cap, sl) in enumerate(MOD_CASES):
+        for dtype in (si.FP64, si.BF16):
+            q = si.normal(80 + n, 1, (B, H, M, D), 2.0, dtype)
+            k = si.normal(80 + n, 2, (B, Hkv, N, D), 2.0, dtype)
+            v = si.normal(80 + n, 3, (B, Hkv, N, D), 1.0, dtype)
+            slopes = None
+            if sl == "h":
+                slopes = 0.5 ** np.arange(1, H + 1)
+            elif sl == "bh":
+                slopes = 0.3 * np.arange(1, B * H + 1).reshape(B, H) / (B * H)
+            o, lse = oracle.attn_fwd_mod(q, k, v, 0.35, causal, window, cap, slopes, lib=lib)
+            ob, lb = brute_force_mod(q, k, v, 0.35, causal, window, cap, slopes)
+            rows = np.array([0, M - 1, B * H * M - 1, (B * H * M) // 3], np.int64)
+            orow, lrow = oracle.attn_fwd_mod(q, k, v, 0.35, causal, window, cap, slopes, rows=rows,
+                                             lib=lib)
+            if not (same(o, ob, 1e-12) and same(lse, lb, 1e-12) and same(orow, o.reshape(-1, D)[rows], 0)
+                    and same(lrow, lse.reshape(-1)[rows], 0)):
+                errs.append(f"mod brute case {n} {dtype}")
+    return errs
+
+
+def mod_reduction_errors(lib):
+    """Modifiers that reduce to plain attention: defaults, a window as wide as
+    the problem, zero slopes, a huge softcap; window (unbounded, 0) == causal."""
+    errs = []
+    B, H, M, N, D = 2, 2, 14, 19, 8
+    q, k, v = rand_inputs(91, B, H, M, N, D, si.FP64)
+    for causal in (False, True):
+        ob, lb = brute_force(q, k, v, 0.4, causal)
+        for kw in (dict(), dict(window=(M, N)), dict(alibi_slopes=np.zeros(H)),
+                   dict(softcap=1e7)):
+            o, lse = oracle.attn_fwd_mod(q, k, v, 0.4, causal, lib=lib, **kw)
+            if not (same(o, ob, 1e-10) and same(lse, lb, 1e-10)):
+                errs.append(f"reduction {sorted(kw)} causal={causal}")
+    ob, lb = brute_force(q, k, v, 0.4, True)
+    o, lse = oracle.attn_fwd_mod(q, k, v, 0.4, False, window=(-1, 0), lib=lib)
+    if not (same(o, ob, 1e-12) and same(lse, lb, 1e-12)):
+        errs.append("window (-1, 0) != causal")
+    return errs
+
+
+def mod_closed_form_errors(lib):
+    errs = []
+    # K = 0 under a window: the mean of the V rows in [i - wl, i + wr] (clipped
+    # to the keys, and to j <= i when causal), L = ln(count); no key: O = 0, L = -inf
+    B, H, M, N, D = 1, 2, 14, 6, 3
+    _, _, v = rand_inputs(92, B, H, M, N, D, si.FP64)
+    for wl, wr in ((0, 0), (2, 1), (3, -1), (-1, 2), (5, 0), (1, 4)):
+        for causal in (False, True):
+            o, lse = oracle.attn_fwd_mod(np.ones((B, H, M, D)), np.zeros((B, H, N, D)), v, 1.0, causal,
+                                         window=(wl, wr), lib=lib)
+            for i in range(M):
+                lo = max(0, i - wl) if wl >= 0 else 0
+                hi = min(N - 1, i + wr) if wr >= 0 else N - 1
+                if causal:
+                    hi = min(hi, i)
+                cnt = hi - lo + 1
+                want_o = v[:, :, lo:hi + 1].mean(axis=2) if cnt > 0 else np.zeros((B, H, D))
+                want_l = math.log(cnt) if cnt > 0 else -math.inf
+                if not (same(o[:, :, i], want_o, 1e-14) and same(lse[:, :, i], np.full((B, H), want_l), 1e-14)):
+                    errs.append(f"K=0 window ({wl},{wr}) causal={causal} row {i}")
+                    break
+    # ALiBi with K = 0 and V = identity: O[i, j] = r^|i-j| / Z_i with r = exp(-a)
+    # and Z_i the two geometric sums to the left and right of i
+    B, H, M, N = 2, 3, 7, 9
+    slopes = np.array([[0.25, 0.5, 1.0], [0.125, 2.0, 0.75]])
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd_mod(np.ones((B, H, M, N)), np.zeros((B, H, N, N)),
+                                     np.broadcast_to(np.eye(N), (B, H, N, N)), 0.5, causal,
+                                     alibi_slopes=slopes, lib=lib)
+        for b in range(B):
+            for h in range(H):
+                r = math.exp(-slopes[b, h])
+                for i in range(M):
+                    left = (1 - r ** (i + 1)) / (1 - r)
+                    right = 0.0 if causal else r * (1 - r ** (N - 1 - i)) / (1 - r)
+                    z = left + right
+                    want = np.array([r ** abs(i - j) / z if (j <= i or not causal) else 0.0
+                                     for j in range(N)])
+                    if not (same(o[b, h, i], want, 1e-14) and abs(lse[b, h, i] - math.log(z)) <= 1e-14):
+                        errs.append(f"ALiBi closed form b={b} h={h} i={i} causal={causal}")
+    # softcap c = 2 on the scores (ln 3, 0): 2 tanh(ln(3)/2) = 1 exactly, so the
+    # capped scores are (1, 0): O = (e v0 + v1) / (e + 1), L = ln(e + 1).  With
+    # ALiBi slope 1 on top (row 0 sees key 1 at distance 1): scores (1, -1).
+    q = np.full((1, 1, 1, 1), math.log(3.0))
+    k = np.array([1.0, 0.0]).reshape(1, 1, 2, 1)
+    v = np.array([3.0, -5.0]).reshape(1, 1, 2, 1)
+    e = math.e
+    o, lse = oracle.attn_fwd_mod(q, k, v, 1.0, False, softcap=2.0, lib=lib)
+    if abs(o.item() - (3 * e - 5) / (e + 1)) > 1e-14 or abs(lse.item() - math.log(e + 1)) > 1e-14:
+        errs.append("softcap closed form")
+    o, lse = oracle.attn_fwd_mod(q, k, v, 1.0, False, softcap=2.0, alibi_slopes=np.ones(1), lib=lib)
+    if abs(o.item() - (3 * e - 5 / e) / (e + 1 / e)) > 1e-14 or abs(lse.item() - math.log(e + 1 / e)) > 1e-14:
+        errs.append("softcap then ALiBi closed form")
+    # saturated softcap: scores 100 and 200 both cap to 5: mean of V, L = 5 + ln 2
+    o, lse = oracle.attn_fwd_mod(np.full((1, 1, 1, 1), 100.0), np.array([1.0, 2.0]).reshape(1, 1, 2, 1),
+                                 v, 1.0, False, softcap=5.0, lib=lib)
+    if abs(o.item() + 1.0) > 1e-14 or abs(lse.item() - (5 + math.log(2))) > 1e-14:
+        errs.append("saturated softcap")
+    return errs
+
+
 def all_pin_errors(lib):
     errs = []
     for check in (golden_errors, brute_errors, large_score_errors, invariant_errors,
-                  rows_errors, tiled_errors, gqa_errors):
+                  rows_errors, tiled_errors, gqa_errors, mod_brute_errors, mod_reduction_errors,
+                  mod_closed_form_errors):
         try:
             errs += check(lib)
         except Exception as exc:  # a mutant may also crash or return an error code
@@ -269,6 +427,18 @@ def test_grouped_query_attention_matches_repeated_heads(oracle_lib):
     assert gqa_errors(oracle_lib) == []
 
 
+def test_score_modifiers_match_brute_force(oracle_lib):
+    assert mod_brute_errors(oracle_lib) == []
+
+
+def test_score_modifiers_reduce_to_plain_attention(oracle_lib):
+    assert mod_reduction_errors(oracle_lib) == []
+
+
+def test_score_modifiers_closed_forms(oracle_lib):
+    assert mod_closed_form_errors(oracle_lib) == []
+
+
 def test_matches_torch_sdpa_fp64():
     torch = pytest.importorskip("torch")
     import torch.nn.functional as F
@@ -319,6 +489,31 @@ MUTANTS = [
      "return (bh / H) * Hkv + (bh % H) % Hkv;", 1),
     ("GQA: batch offset of the K/V head dropped", "return (bh / H) * Hkv + (bh % H) / (H / Hkv);",
      "return (bh % H) / (H / Hkv);", 1),
+    ("window: left bound one key short", "if (wl >= 0 && i - wl > lo) lo = i - wl;",
+     "if (wl >= 0 && i - wl > lo) lo = i - wl + 1;", 1),
+    ("window: right bound one key long", "if (wr >= 0 && i + wr < hi) hi = i + wr;",
+     "if (wr >= 0 && i + wr < hi) hi = i + wr + 1;", 1),
+    ("window: causal ignored", "if (causal && i < hi) hi = i;", "if (0 && i < hi) hi = i;", 1),
+    ("window: V rows read from the window start", "acc += w[j - lo] * widen(v, kvoff + j * D + d, dtype);",
+     "acc += w[j - lo] * widen(v, kvoff + (j - lo) * D + d, dtype);", 1),
+    ("window: empty row L = 0", "    *lse = -INFINITY;\n    return 0;", "    *lse = 0.0;\n    return 0;", 1),
+    ("softcap: inner divide dropped", "s = softcap * tanh(s / softcap);", "s = softcap * tanh(s);", 1),
+    ("softcap: outer multiply dropped", "s = softcap * tanh(s / softcap);", "s = tanh(s / softcap);", 1),
+    ("ALiBi: sign flipped", "s -= slope * fabs((double)(i - j));", "s += slope * fabs((double)(i - j));", 1),
+    ("ALiBi: signed distance", "s -= slope * fabs((double)(i - j));", "s -= slope * (double)(i - j);", 1),
+    ("ALiBi: every head uses slope 0", "slopes[(bh / H) * slope_bstride + bh % H]",
+     "slopes[(bh / H) * slope_bstride]", 1),
+    ("ALiBi: batch stride ignored", "slopes[(bh / H) * slope_bstride + bh % H]", "slopes[bh % H]", 1),
+    ("ALiBi: added before the softcap", "    if (softcap > 0.0) s = softcap * tanh(s / softcap);\n"
+     "    s -= slope * fabs((double)(i - j));",
+     "    s -= slope * fabs((double)(i - j));\n    if (softcap > 0.0) s = softcap * tanh(s / softcap);", 1),
+    ("mod: Q row offset dropped", "const int64_t qoff = (bh * M + i) * (int64_t)D;\n  int64_t lo",
+     "const int64_t qoff = (bh * M) * (int64_t)D;\n  int64_t lo", 1),
+    ("mod: K/V head offset dropped", "const int64_t kvoff = kvh * (int64_t)N * D;\n  const int64_t qoff",
+     "const int64_t kvoff = 0;\n  const int64_t qoff", 1),
+    ("mod: no final divide", "o_row[d] = acc / lsum;", "o_row[d] = acc;", 1),
+    ("mod: L missing max", "*lse = m + log(lsum);", "*lse = log(lsum);", 1),
+    ("mod: max not subtracted", "w[j - lo] = exp(w[j - lo] - m);", "w[j - lo] = exp(w[j - lo]);", 1),
     ("tiled: O not rescaled", "acc[(int64_t)r * D + d] = alpha * acc[(int64_t)r * D + d] + pv;",
      "acc[(int64_t)r * D + d] = acc[(int64_t)r * D + d] + pv;", 1),
     ("tiled: l not rescaled", "l_run[r] = alpha * l_run[r] + rowsum;", "l_run[r] = l_run[r] + rowsum;", 1),
