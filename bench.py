@@ -201,20 +201,27 @@ def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
     import oracle
     rng = np.random.default_rng(seed)
     total_rows = w.B * w.H * w.M
+
+    def run(rows):
+        if w.modified:
+            oracle.attn_fwd_mod(q, k, v, w.scale, w.causal, w.window, w.softcap,
+                                si.alibi_slopes(w.H).astype(np.float64) if w.alibi else None,
+                                rows=rows)
+        else:
+            oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
+
     rows = np.sort(rng.choice(total_rows, size=64, replace=False))
-    oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows[:8])  # warm (build, pages)
+    run(rows[:8])  # warm (build, pages)
     n = 64
     while True:
         rows = np.sort(rng.choice(total_rows, size=n, replace=False))
         t0 = time.perf_counter()
-        oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
+        run(rows)
         dt = time.perf_counter() - t0
         if dt >= seconds_target or n >= total_rows:
             break
         n = min(total_rows, int(n * max(2.0, 1.2 * seconds_target / max(dt, 1e-3))))
-    i = rows % w.M
-    nvis = np.minimum(i + 1, w.N) if w.causal else np.full(rows.shape, w.N)
-    flops = float(np.sum(4.0 * w.D * nvis))
+    flops = float(np.sum(4.0 * w.D * w.visible_keys(rows % w.M)))
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     omp = os.environ.get("OMP_NUM_THREADS")
     cores = int(omp) if omp else cores
@@ -307,7 +314,13 @@ def run_ours(args, rank, local, world):
     stream = torch.cuda.current_stream(dev)
 
     launches_per_step = 1
-    if w.split_kv:
+    if w.modified:
+        slopes = torch.from_numpy(si.alibi_slopes(w.H)).to(dev) if w.alibi else None
+
+        def step():
+            fa2.fa2_fwd_ext(tq, tk, tv, o=o, lse=lse, scale=w.scale, causal=w.causal, window=w.window,
+                            softcap=w.softcap, alibi_slopes=slopes, num_splits=1, stream=stream)
+    elif w.split_kv:
         dcode = fa2.FA2_BF16 if w.dtype == si.BF16 else fa2.FA2_FP32
         n_split = fa2.fa2_splitkv_num_splits(w.B, w.H, w.M, w.N, w.D, dcode)
         ws = torch.empty(max(256, fa2.fa2_splitkv_workspace_bytes(w.B, w.H, w.M, w.D, n_split)),
@@ -368,7 +381,9 @@ def run_ours(args, rank, local, world):
                    "D": w.D, "causal": w.causal, "scale": w.scale,
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}",
-                   **({"num_splits": n_split} if w.split_kv else {})},
+                   **({"num_splits": n_split} if w.split_kv else {}),
+                   **({"window": list(w.window), "softcap": w.softcap, "alibi": w.alibi}
+                      if w.modified else {})},
         "frac_of_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,

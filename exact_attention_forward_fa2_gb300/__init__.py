@@ -29,6 +29,7 @@ FA2_ERR_ARCH = -8
 FA2_ERR_CUDA = -9
 FA2_ERR_DEVICE_TIMEOUT = -10
 FA2_ERR_WORKSPACE = -11
+FA2_ERR_MODIFIER = -12
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa2_gb300.so")
 
@@ -41,6 +42,8 @@ SIGNATURES = {
                          _VP], _I),
     "fa2_fwd_splitkv_noalloc": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I,
                                  _VP], _I),
+    "fa2_fwd_ext": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _F, _VP, _I, _I,
+                     _I, _VP, _SZ, _VP], _I),
     "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I], _I),
     "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "fa2_strerror": ([_I], ctypes.c_char_p),
@@ -172,6 +175,53 @@ def fa2_fwd_splitkv(q, k, v, o=None, lse=None, scale: float | None = None, causa
                                    _stream_handle(q, stream))
     if rc != FA2_OK:
         raise Fa2Error(rc, "fa2_fwd_splitkv")
+    return o, lse
+
+
+def fa2_fwd_ext(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,
+                window=(-1, -1), softcap: float = 0.0, alibi_slopes=None, num_splits: int = 1,
+                workspace=None, stream=None):
+    """Forward with score modifiers (C ABI ``fa2_fwd_ext``): ``window`` =
+    (left, right) keys a row may see before / after its diagonal, negative =
+    unbounded; ``softcap`` > 0 caps scores at softcap * tanh(s / softcap);
+    ``alibi_slopes`` (fp32 CUDA tensor [H] or [B, H]) subtracts slope * |i - j|.
+    ``num_splits`` as in fa2_fwd_splitkv (1 = no key split, 0 = the library's
+    choice); the workspace is allocated with torch when needed and not given."""
+    import torch
+
+    dtype = _check_qkv(q, k, v)
+    B, H, M, D = q.shape
+    H_kv, N = k.shape[1], k.shape[2]
+    o, lse = _outputs(q, o, lse)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    slopes_ptr, stride = None, 0
+    if alibi_slopes is not None:
+        if alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_contiguous() \
+                or alibi_slopes.device != q.device:
+            raise ValueError("alibi_slopes must be a contiguous fp32 tensor on q's device")
+        if tuple(alibi_slopes.shape) == (H,):
+            stride = 0
+        elif tuple(alibi_slopes.shape) == (B, H):
+            stride = H
+        else:
+            raise ValueError("alibi_slopes must have shape [H] or [B, H]")
+        slopes_ptr = alibi_slopes.data_ptr()
+    wl, wr = (int(x) for x in window)
+    with torch.cuda.device(q.device):
+        if num_splits <= 0:
+            num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype)
+        need = fa2_splitkv_workspace_bytes(B, H, M, D, num_splits)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        rc = lib().fa2_fwd_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, H_kv, M, N, D, float(scale),
+                               1 if causal else 0, wl, wr, float(softcap), slopes_ptr, stride,
+                               dtype, num_splits, ws_ptr, ws_len, _stream_handle(q, stream))
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_fwd_ext")
     return o, lse
 
 

@@ -121,11 +121,21 @@ size_t workspace_bytes(int64_t rows, int D, int splits) {
   return lpart_offset(rows, D, splits) + static_cast<size_t>(splits) * rows * sizeof(float);
 }
 
+// Score modifiers of fa2_fwd_ext; the defaults leave the plain forward.
+struct Modifiers {
+  int window_left = -1;   // < 0: no left bound
+  int window_right = -1;  // < 0: no right bound
+  float softcap = 0.f;    // 0: no softcap
+  const float* alibi = nullptr;
+  int alibi_bstride = 0;
+};
+
 // Shared by every entry point.  num_splits == 1: plain forward; > 1: split-KV
 // partials into `workspace`, then the combine kernel.
 int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int H_kv, int M, int N, int D, float scale, int causal, int dtype, int num_splits,
-                void* workspace, size_t workspace_size, void* stream) {
+                void* workspace, size_t workspace_size, void* stream,
+                const Modifiers& mods = Modifiers()) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
   if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
@@ -135,6 +145,14 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
   if ((addr(q) | addr(k) | addr(v) | addr(o)) & 15u) return FA2_ERR_ALIGN;
   if (addr(lse) & 3u) return FA2_ERR_ALIGN;
+  if (!(mods.softcap >= 0.f) || std::isinf(mods.softcap)) return FA2_ERR_MODIFIER;
+  if (mods.alibi && mods.alibi_bstride != 0 && mods.alibi_bstride != H) return FA2_ERR_MODIFIER;
+  if (addr(mods.alibi) & 3u) return FA2_ERR_ALIGN;
+  // a causal right edge is the diagonal whatever window_right says
+  const bool use_mod = mods.window_left >= 0 || (!causal && mods.window_right >= 0) ||
+                       mods.softcap > 0.f || mods.alibi != nullptr;
+  // the kernel forms row +- window and key - row in 32-bit ints and fp32
+  if (use_mod && (M > (1 << 30) || N > (1 << 30))) return FA2_ERR_TOO_LARGE;
   const int64_t bh = static_cast<int64_t>(B) * H;
   const int64_t bh_kv = static_cast<int64_t>(B) * H_kv;
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
@@ -183,7 +201,17 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
                                                    lpart_offset(rows, D, num_splits))
                         : nullptr;
   L.params.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  // window bounds: an absent side widens to cover every key (row - M <= 0 and
+  // row + N >= N - 1 for every row); causal caps the right side at the diagonal
+  L.params.win_left = (mods.window_left < 0 || mods.window_left > M) ? M : mods.window_left;
+  L.params.win_right = (mods.window_right < 0 || mods.window_right > N) ? N : mods.window_right;
+  if (causal) L.params.win_right = 0;
+  L.params.cap_in = mods.softcap > 0.f ? static_cast<float>(static_cast<double>(scale) / mods.softcap) : 0.f;
+  L.params.cap_out = static_cast<float>(static_cast<double>(mods.softcap) * 1.4426950408889634);
+  L.params.alibi = mods.alibi;
+  L.params.alibi_bstride = mods.alibi_bstride;
   L.causal = causal ? 1 : 0;
+  L.mod = use_mod ? 1 : 0;
   L.stream = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -245,6 +273,26 @@ extern "C" int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void
                      workspace, workspace_size, stream);
 }
 
+extern "C" int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int H_kv, int M, int N, int D, float scale, int causal,
+                           int window_left, int window_right, float softcap,
+                           const float* alibi_slopes, int alibi_batch_stride, int dtype,
+                           int num_splits, void* workspace, size_t workspace_size, void* stream) {
+  if (num_splits <= 0) {
+    num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype);
+    if (num_splits < 0) return num_splits;
+  }
+  if (num_splits > kMaxSplits) num_splits = kMaxSplits;
+  Modifiers mods;
+  mods.window_left = window_left;
+  mods.window_right = window_right;
+  mods.softcap = softcap;
+  mods.alibi = alibi_slopes;
+  mods.alibi_bstride = alibi_batch_stride;
+  return run_forward(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, causal, dtype, num_splits,
+                     workspace, workspace_size, stream, mods);
+}
+
 extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int M, int N, int D, float scale, int causal, int dtype,
                        void* stream) {
@@ -265,6 +313,7 @@ extern "C" const char* fa2_strerror(int status) {
     case FA2_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case FA2_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait ran out of time";
     case FA2_ERR_WORKSPACE: return "split-KV workspace missing, not 256-byte aligned or too small";
+    case FA2_ERR_MODIFIER: return "softcap must be finite and >= 0, alibi_batch_stride 0 or H";
     default: return "unknown status";
   }
 }
@@ -284,4 +333,4 @@ extern "C" int fa2_device_status(int reset, int* raw_code) {
   return word == 0 ? FA2_OK : FA2_ERR_DEVICE_TIMEOUT;
 }
 
-extern "C" int fa2_version(void) { return 100; }
+extern "C" int fa2_version(void) { return 200; }

@@ -54,6 +54,16 @@ struct FwdParams {
   int tiles_per_split;
   float* o_part;        // [num_splits][BH][M][D] fp32 (num_splits > 1)
   float* l_part;        // [num_splits][BH][M] fp32 (num_splits > 1)
+  // score modifiers, read by the kMod instantiations only: key j is visible to
+  // query row i iff i - win_left <= j <= i + win_right (the host folds the causal
+  // bound into win_right and widens an unbounded side to cover every key);
+  // s <- cap_out * tanh(s * cap_in) in log2 units when cap_in > 0 (softcap);
+  // s <- s - log2(e) * slope * |i - j| when alibi is not null (ALiBi)
+  int win_left, win_right;
+  float cap_in;         // scale / softcap, 0 = no softcap
+  float cap_out;        // softcap * log2(e)
+  const float* alibi;   // slopes, read at b * alibi_bstride + h; null = no ALiBi
+  int alibi_bstride;
 };
 
 // Device status codes (first failing wait site wins).
@@ -153,12 +163,42 @@ __device__ __forceinline__ int kv_tiles_for(int row0, int M, int N, bool causal)
   return min(total, last_row / 128 + 1);
 }
 
-// Key tiles of that query tile inside split `split` (tiles [split*tps, +tps)):
-// the count; the first one is split*tps.
-__device__ __forceinline__ int kv_tiles_in_split(int row0, const FwdParams& p, bool causal,
-                                                 int split) {
-  const int n = kv_tiles_for(row0, p.M, p.N, causal) - split * p.tiles_per_split;
-  return max(0, min(n, p.tiles_per_split));
+// Key tiles [first, first + count) that the query tile starting at row0 visits
+// inside split `split` (key tiles [split*tps, +tps)); count 0 = nothing to do.
+// Plain: every key tile, or up to the diagonal when causal; the first is the
+// split's first tile.  kMod: the tiles holding keys [row0 - win_left,
+// last row + win_right] (a sliding window; the causal bound is in win_right).
+struct KvSpan {
+  int first, count;
+};
+
+template <bool kMod>
+__device__ __forceinline__ KvSpan kv_span(int row0, const FwdParams& p, bool causal, int split) {
+  const int s0 = split * p.tiles_per_split;
+  if constexpr (!kMod) {
+    const int n = kv_tiles_for(row0, p.M, p.N, causal) - s0;
+    return KvSpan{s0, max(0, min(n, p.tiles_per_split))};
+  } else {
+    KvSpan r{s0, 0};
+    if (row0 >= p.M) return r;
+    const int last_row = min(row0 + 128, p.M) - 1;
+    const int first_key = max(0, row0 - p.win_left);
+    const int last_key = min(p.N - 1, last_row + p.win_right);
+    if (first_key > last_key) return r;
+    const int lo = max(first_key / 128, s0), hi = min(last_key / 128 + 1, s0 + p.tiles_per_split);
+    if (hi > lo) {
+      r.first = lo;
+      r.count = hi - lo;
+    }
+    return r;
+  }
+}
+
+// tanh(x) = sign(x) (1 - e^(-2|x|)) / (1 + e^(-2|x|)), with e^(-2|x|) from ex2:
+// the quotient never overflows, and near 0 its absolute error stays ~1e-7.
+__device__ __forceinline__ float tanh_ex2(float x) {
+  const float t = ptx::ex2_approx(-2.8853900817779268f * fabsf(x));  // 2 log2(e)
+  return copysignf(__fdividef(1.0f - t, 1.0f + t), x);
 }
 
 struct WaitCtx {
@@ -192,7 +232,7 @@ __device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <class C, bool kCausal>
+template <class C, bool kCausal, bool kMod>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -216,13 +256,33 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   // key/value head read by this query head (grouped-query attention, "From
   // FlashAttention to FlashAttention 2", Layer 8: h_kv = h / (H / H_kv))
   const int bh_kv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
-  int row0[C::kQTiles], nkv[C::kQTiles];
-  int n_max = 0;
+  // Query tile t visits key tiles [kt0[t], kt0[t] + nkv[t]); the CTA streams key
+  // tiles ks, ks + 1, ..., ks + n_max - 1 and tile t uses stream positions
+  // [jb[t], jb[t] + nkv[t]).  Without a window every tile starts at the split's
+  // first key tile, so jb is 0.
+  int row0[C::kQTiles], kt0[C::kQTiles], nkv[C::kQTiles], jb[C::kQTiles];
+  int ks = kb, n_max = 0;
 #pragma unroll
   for (int t = 0; t < C::kQTiles; ++t) {
     row0[t] = (unit.pair * C::kQTiles + t) * C::BM;
-    nkv[t] = kv_tiles_in_split(row0[t], p, kCausal, split);
+    const KvSpan sp = kv_span<kMod>(row0[t], p, kCausal, split);
+    kt0[t] = sp.first;
+    nkv[t] = sp.count;
+    jb[t] = 0;
     n_max = max(n_max, nkv[t]);
+  }
+  if constexpr (kMod) {
+    int lo = 0x7fffffff, hi = 0;
+#pragma unroll
+    for (int t = 0; t < C::kQTiles; ++t)
+      if (nkv[t] > 0) {
+        lo = min(lo, kt0[t]);
+        hi = max(hi, kt0[t] + nkv[t]);
+      }
+    ks = hi > 0 ? lo : 0;
+    n_max = hi > 0 ? hi - lo : 0;
+#pragma unroll
+    for (int t = 0; t < C::kQTiles; ++t) jb[t] = kt0[t] - ks;
   }
 
   // ------------------------------------------------------------ set-up
@@ -285,7 +345,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffK + s * C::kTileBytes + cb * C::kBlockBytes, &tmK,
-                           bar(C::kBarKFull + s), cb * C::kSwElems, (kb + j) * C::BN, bh_kv, pol_kv);
+                           bar(C::kBarKFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
         if (use > 0 && !wait_bounded(bar(C::kBarVEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaV)) {
           issued = -(j + 1);  // K_j issued, V_j not
           break;
@@ -294,7 +354,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffV + s * C::kTileBytes + cb * C::kBlockBytes, &tmV,
-                           bar(C::kBarVFull + s), cb * C::kSwElems, (kb + j) * C::BN, bh_kv, pol_kv);
+                           bar(C::kBarVFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
         issued = j + 1;
       }
       if (*wctx.abort_flag) {
@@ -322,11 +382,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int t = 0; t < C::kQTiles; ++t) {
-          if (j >= 1 && j - 1 < nkv[t]) {
+          if ((kMod ? j - 1 >= jb[t] : j >= 1) && j - 1 < jb[t] + nkv[t]) {
             // O_t += P_t V_{j-1}
             const int jp = j - 1;
             const int sv = jp % C::kStages;
-            ok = wait_bounded(bar(C::kBarPFull + t), jp & 1, wctx, kStatusTimeoutMmaP);
+            ok = wait_bounded(bar(C::kBarPFull + t), (kMod ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
             if (!ok) break;
             if (!v_ready) {
               ok = wait_bounded(bar(C::kBarVFull + sv), (jp / C::kStages) & 1, wctx, kStatusTimeoutMmaV);
@@ -335,6 +395,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             }
             tc_fence_after_sync();
             const uint32_t v_base = base + C::kOffV + sv * C::kTileBytes;
+            const int jp0 = kMod ? jb[t] : 0;  // first P V of this tile overwrites O
 #pragma unroll
             for (int kk = 0; kk < C::kStepsPV; ++kk) {
               // B = V rows [kk*kMmaK, +kMmaK), all D columns, MN-major
@@ -343,13 +404,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                            : smem_desc(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 512, kLayoutSw128Atom32);
               const uint32_t a_tmem = tmem + C::kColS(t) + kk * 8;
               if constexpr (C::kBF16)
-                mma_f16_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
+                mma_f16_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
               else
-                mma_tf32_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > 0 || kk > 0) ? 1u : 0u);
+                mma_tf32_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
             }
             tc_commit(bar(C::kBarOFull + t));
           }
-          if (j < nkv[t]) {
+          if ((kMod ? j >= jb[t] : true) && j < jb[t] + nkv[t]) {
             // S_t = Q_t K_j^T
             if (!k_ready) {
               ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
@@ -373,6 +434,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         if (!ok) break;
+        if constexpr (kMod) {
+          // a ring slot is handed back only after its copy landed, even if no
+          // query tile of this CTA read it
+          if (j >= 1 && !v_ready)
+            ok = wait_bounded(bar(C::kBarVFull + (j - 1) % C::kStages), ((j - 1) / C::kStages) & 1, wctx,
+                              kStatusTimeoutMmaV);
+          if (ok && j < n_max && !k_ready)
+            ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
+          if (!ok) break;
+        }
         if (j >= 1) tc_commit(bar(C::kBarVEmpty + (j - 1) % C::kStages));
         if (j < n_max) tc_commit(bar(C::kBarKEmpty + s));
       }
@@ -387,11 +458,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
     const int tile_row0 = (unit.pair * C::kQTiles + t) * C::BM;
     const int row = tile_row0 + r;
-    const int n_t = kv_tiles_in_split(tile_row0, p, kCausal, split);
+    const KvSpan span = kv_span<kMod>(tile_row0, p, kCausal, split);
+    const int n_t = span.count;
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS(t);
     const uint32_t tO = tmem + lane_addr + C::kColO(t);
-    const float sl2 = p.scale_log2;
+    // kMod turns S into log2 units before the max, so the exponent step multiplies by 1
+    const float sl2 = kMod ? 1.0f : p.scale_log2;
+    float slope2 = 0.f;  // ALiBi slope * log2(e) of this head
+    if constexpr (kMod) {
+      if (p.alibi != nullptr)
+        slope2 = p.alibi[(bh / p.H) * p.alibi_bstride + bh % p.H] * 1.4426950408889634f;
+    }
     const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
     float m_run = -INFINITY;  // exponent base in use: a running max of scale*log2e*s
     float l_run = 0.f;        // running sum of the rounded exp2(s*sl2 - m_run)
@@ -411,14 +489,39 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       float s[C::BN];
 #pragma unroll
       for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
-      // mask keys past N and, when causal, keys after this row (boundary tiles only)
-      const int key0 = (kb + j) * C::BN;
-      const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
-      if (boundary) {
-        int lim = p.N - 1 - key0;
-        if (kCausal) lim = min(lim, row - key0);
+      const int key0 = ((kMod ? span.first : kb) + j) * C::BN;
+      if constexpr (kMod) {
+        // score modifiers in log2 units: softcap, then the ALiBi distance penalty
+        if (p.cap_in > 0.f) {
 #pragma unroll
-        for (int c = 0; c < C::BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+          for (int c = 0; c < C::BN; ++c) s[c] = p.cap_out * tanh_ex2(s[c] * p.cap_in);
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) s[c] *= p.scale_log2;
+        }
+        if (slope2 != 0.f) {
+          const float d0 = static_cast<float>(key0 - row);
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) s[c] = fmaf(-slope2, fabsf(d0 + static_cast<float>(c)), s[c]);
+        }
+        // window mask, on tiles that cross N or either window edge of some row
+        const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||
+                              (key0 < tile_row0 + C::BM - 1 - p.win_left);
+        if (boundary) {
+          const int hi = min(p.N - 1, row + p.win_right) - key0;
+          const int lo = row - p.win_left - key0;
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) s[c] = (c >= lo && c <= hi) ? s[c] : -INFINITY;
+        }
+      } else {
+        // mask keys past N and, when causal, keys after this row (boundary tiles only)
+        const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
+        if (boundary) {
+          int lim = p.N - 1 - key0;
+          if (kCausal) lim = min(lim, row - key0);
+#pragma unroll
+          for (int c = 0; c < C::BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+        }
       }
       // row max: four independent chains of 3-input max
       float mx[4] = {s[0], s[1], s[2], s[3]};
@@ -540,13 +643,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           p.l_part[prow] = -INFINITY;
         }
       }
-    } else if (n_t > 0) {
+    } else if (n_t > 0 || (kMod && tile_row0 < p.M)) {
+      // (kMod: a window can leave every row of a tile without a visible key; the
+      // tile is then written as O = 0, L = -inf)
       if (ok)
         ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
                                                   kStatusTimeoutEpilogue));
       // Q_t's shared tile is free once the last GEMM of this tile completed: stage O there
       const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
-      if (ok) {
+      if (kMod && n_t == 0) {
+#pragma unroll
+        for (int cidx = 0; cidx < C::kColBlocks * 8; ++cidx)
+          st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
+        if (row < p.M) p.lse[static_cast<int64_t>(bh) * p.M + row] = -INFINITY;
+      } else if (ok) {
         tc_fence_after_sync();
         const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll
@@ -612,6 +722,7 @@ struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmO;
   FwdParams params;
   int causal;
+  int mod;  // score modifiers in use (window, softcap or ALiBi): the kMod kernels
   cudaStream_t stream;
 };
 

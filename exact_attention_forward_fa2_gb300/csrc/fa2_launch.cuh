@@ -1,40 +1,42 @@
-// Launch side of the forward kernel: one instantiation unit per (dtype, D)
-// includes this file and defines its entry through FA2_DEFINE_LAUNCH.
+// Launch side of the forward kernel: each instantiation unit (one per dtype and
+// head dim) includes this file and calls launch_cfg with its tile configuration.
 #pragma once
 
 #include "fa2_fwd_kernel.cuh"
 
 namespace fa2 {
 
-// Sets the dynamic shared-memory limit once per device, then launches one CTA
-// per work unit on the caller's stream.
-template <class C>
-cudaError_t launch_cfg(FwdLaunch& L) {
-  static bool attr_done[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(fa2_fwd_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
+// Sets the dynamic shared-memory limit once per device and kernel, then launches
+// one CTA per (work unit, key split) on the caller's stream.
+template <class C, bool kCausal, bool kMod>
+cudaError_t launch_one(FwdLaunch& L, bool& attr_done) {
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(fa2_fwd_kernel<C, kCausal, kMod>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fa2_fwd_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done = true;
   }
-  L.params.units_per_head = (L.params.M + C::kQTiles * C::BM - 1) / (C::kQTiles * C::BM);
-  L.params.num_units = L.params.units_per_head * L.params.BH;
   const dim3 grid(static_cast<unsigned>(L.params.num_units * L.params.num_splits));
   const dim3 block(C::kThreads);
-  if (L.causal)
-    fa2_fwd_kernel<C, true><<<grid, block, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmO,
-                                                                       L.params);
-  else
-    fa2_fwd_kernel<C, false><<<grid, block, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmO,
-                                                                        L.params);
+  fa2_fwd_kernel<C, kCausal, kMod><<<grid, block, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV,
+                                                                            L.tmO, L.params);
   return cudaGetLastError();
+}
+
+template <class C>
+cudaError_t launch_cfg(FwdLaunch& L) {
+  static bool attr_done[64][4] = {};
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  L.params.units_per_head = (L.params.M + C::kQTiles * C::BM - 1) / (C::kQTiles * C::BM);
+  L.params.num_units = L.params.units_per_head * L.params.BH;
+  bool* done = attr_done[dev];
+  if (L.mod)
+    return L.causal ? launch_one<C, true, true>(L, done[3]) : launch_one<C, false, true>(L, done[2]);
+  return L.causal ? launch_one<C, true, false>(L, done[1]) : launch_one<C, false, false>(L, done[0]);
 }
 
 }  // namespace fa2

@@ -56,6 +56,7 @@ extern "C" {
 #define FA2_ERR_CUDA (-9)           /* a CUDA runtime or driver call failed */
 #define FA2_ERR_DEVICE_TIMEOUT (-10) /* a kernel gave up on a pipeline wait (see fa2_device_status) */
 #define FA2_ERR_WORKSPACE (-11)     /* split-KV workspace missing, misaligned or too small */
+#define FA2_ERR_MODIFIER (-12)      /* softcap < 0 or not finite, or alibi_batch_stride not 0 or H */
 
 /*
  * fa2_fwd -- FlashAttention-2 forward pass.
@@ -143,6 +144,41 @@ size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits);
 int fa2_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int H_kv, int M, int N, int D, float scale, int causal,
                             int dtype, int num_splits, void* stream);
+
+/*
+ * fa2_fwd_ext -- the forward pass with score modifiers: a sliding window, a
+ * softcap and ALiBi biases ("From FlashAttention to FlashAttention 2", Layer 1:
+ * Python API, the window_size, softcap and alibi_slopes options; "Writing
+ * FlashAttention 2 in Triton", What to do after your FA2 works: the sliding-window
+ * mask as a change of the causal mask formula, ALiBi as a bias added to the
+ * score).  For query row i of head (b, h) and key j:
+ *     s = scale * q_i . k_j
+ *     s = softcap * tanh(s / softcap)                     when softcap > 0
+ *     s = s - alibi_slopes[b * alibi_batch_stride + h] * |i - j|
+ *                                                         when alibi_slopes != NULL
+ * and key j is visible iff j < N, j >= i - window_left (when window_left >= 0),
+ * j <= i + window_right (when window_right >= 0) and j <= i (when causal).  O and
+ * L are the softmax-weighted sum and the logsumexp of s over the visible keys; a
+ * row with no visible key (possible with a window) gets O = 0 and L = -inf.
+ *
+ *   window_left, window_right  keys before / after the diagonal a row may see;
+ *                      negative = unbounded (-1, -1: no window)
+ *   softcap            0 = off; otherwise finite and > 0
+ *   alibi_slopes       NULL = no ALiBi, or a DEVICE fp32 array (4-byte aligned,
+ *                      caller-owned, only read) of H slopes shared by every batch
+ *                      entry (alibi_batch_stride 0) or B*H slopes (stride H)
+ *   num_splits, workspace, workspace_size   as fa2_fwd_splitkv: 1 = no key
+ *                      split (workspace unused), <= 0 = the library's choice
+ * Other arguments, layouts and errors as fa2_fwd_gqa, plus FA2_ERR_MODIFIER for an
+ * invalid softcap or stride, FA2_ERR_ALIGN for misaligned slopes and
+ * FA2_ERR_TOO_LARGE when a modifier is in use and M or N exceeds 2^30.  With no
+ * modifier in use this is fa2_fwd_splitkv.
+ */
+int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int H_kv, int M, int N, int D, float scale, int causal, int window_left,
+                int window_right, float softcap, const float* alibi_slopes,
+                int alibi_batch_stride, int dtype, int num_splits, void* workspace,
+                size_t workspace_size, void* stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);

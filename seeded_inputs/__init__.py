@@ -114,6 +114,9 @@ class Workload:
     sigma_v: float = 1.0
     H_kv: int = 0  # key/value heads (grouped-query attention); 0 means H
     split_kv: bool = False  # measured through the split-KV entry
+    window: tuple = (-1, -1)  # (left, right) sliding window; negative = unbounded
+    softcap: float = 0.0  # 0 = no softcap
+    alibi: bool = False  # ALiBi with alibi_slopes(H)
 
     @property
     def Hkv(self) -> int:
@@ -124,8 +127,27 @@ class Workload:
         return 1.0 / float(np.sqrt(self.D))
 
     @property
+    def modified(self) -> bool:
+        """A score modifier (window, softcap or ALiBi) is in use."""
+        return self.window != (-1, -1) or self.softcap > 0 or self.alibi
+
+    def visible_keys(self, i) -> np.ndarray:
+        """Keys visible to query rows i (array), under the mask and window."""
+        i = np.asarray(i, np.int64)
+        lo = np.maximum(0, i - self.window[0]) if self.window[0] >= 0 else np.zeros_like(i)
+        hi = np.full_like(i, self.N - 1)
+        if self.window[1] >= 0:
+            hi = np.minimum(hi, i + self.window[1])
+        if self.causal:
+            hi = np.minimum(hi, i)
+        return np.maximum(0, hi - lo + 1)
+
+    @property
     def flops(self) -> float:
-        """4*B*H*M*N*D, halved for causal (the pages' attention FLOP count)."""
+        """4*B*H*M*N*D, halved for causal (the pages' attention FLOP count); with
+        a window, 4*D per visible (query, key) pair."""
+        if self.window != (-1, -1):
+            return 4.0 * self.B * self.H * self.D * float(np.sum(self.visible_keys(np.arange(self.M))))
         f = 4.0 * self.B * self.H * self.M * self.N * self.D
         return f / 2 if self.causal else f
 
@@ -153,7 +175,21 @@ WORKLOADS = {
     # cache): 32 query-tile units cannot fill the GPU, so the key range is split
     "bf16_1x32x128x32768x128_gqa8_splitkv": Workload("bf16_1x32x128x32768x128_gqa8_splitkv", 1, 32, 128, 32768, 128,
                                                      BF16, False, 7, H_kv=8, split_kv=True),
+    # score modifiers at the headline size: a 2048-key causal sliding window, a
+    # softcap of 50, ALiBi with the geometric slopes below
+    "bf16_2x16x8192x8192x128_causal_window2048": Workload("bf16_2x16x8192x8192x128_causal_window2048", 2, 16, 8192,
+                                                          8192, 128, BF16, True, 8, window=(2048, -1)),
+    "bf16_2x16x8192x8192x128_causal_softcap50": Workload("bf16_2x16x8192x8192x128_causal_softcap50", 2, 16, 8192,
+                                                         8192, 128, BF16, True, 9, softcap=50.0),
+    "bf16_2x16x8192x8192x128_causal_alibi": Workload("bf16_2x16x8192x8192x128_causal_alibi", 2, 16, 8192, 8192,
+                                                     128, BF16, True, 10, alibi=True),
 }
+
+
+def alibi_slopes(H: int) -> np.ndarray:
+    """ALiBi slopes, one per head: the geometric sequence 2^(-8 (h + 1) / H),
+    fp32 (an input of the method, like Q, K and V)."""
+    return (2.0 ** (-8.0 * np.arange(1, H + 1) / H)).astype(np.float32)
 
 
 def make_qkv(w: Workload):

@@ -31,7 +31,7 @@ def lib():
 
 
 def test_header_declares_the_api():
-    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_fwd_gqa", "fa2_fwd_splitkv",
+    assert declared_functions() == ["fa2_device_status", "fa2_fwd", "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_splitkv",
                                     "fa2_fwd_splitkv_noalloc", "fa2_splitkv_num_splits",
                                     "fa2_splitkv_workspace_bytes", "fa2_strerror", "fa2_version"]
 
@@ -129,6 +129,28 @@ def test_splitkv_validates_like_fa2_fwd(lib):
     assert call_split(lib, q=None) == fa2.FA2_ERR_NULL
     assert call_split(lib, H_kv=3) == fa2.FA2_ERR_SHAPE
     assert call_split(lib, D=32) == fa2.FA2_ERR_HEADDIM
+
+
+def call_ext(lib, window=(-1, -1), softcap=0.0, slopes=None, stride=0, num_splits=1, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=2, H=4, H_kv=2, M=8, N=300, D=64, scale=0.125, causal=0,
+             dtype=0)
+    a.update(kw)
+    return lib.fa2_fwd_ext(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["H_kv"], a["M"],
+                           a["N"], a["D"], a["scale"], a["causal"], window[0], window[1], softcap,
+                           slopes, stride, a["dtype"], num_splits, None, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(softcap=-1.0), fa2.FA2_ERR_MODIFIER), (dict(softcap=float("inf")), fa2.FA2_ERR_MODIFIER),
+    (dict(softcap=float("nan")), fa2.FA2_ERR_MODIFIER),
+    (dict(slopes=P, stride=3), fa2.FA2_ERR_MODIFIER), (dict(slopes=P, stride=-4), fa2.FA2_ERR_MODIFIER),
+    (dict(slopes=P + 2), fa2.FA2_ERR_ALIGN),
+    (dict(window=(5, 5), M=(1 << 30) + 1), fa2.FA2_ERR_TOO_LARGE),
+    (dict(window=(5, 5), q=None), fa2.FA2_ERR_NULL), (dict(softcap=30.0, D=96), fa2.FA2_ERR_HEADDIM),
+    (dict(window=(5, 5), num_splits=4), fa2.FA2_ERR_WORKSPACE),
+])
+def test_ext_rejects_bad_arguments(lib, kw, code):
+    assert call_ext(lib, **kw) == code
 
 
 def test_no_gpu_means_an_error_not_a_fallback(lib):

@@ -1,0 +1,166 @@
+"""GPU parity of the score modifiers (fa2_fwd_ext: sliding window, softcap,
+ALiBi) against the fp64 oracle's attn_fwd_mod on the same seeded inputs.
+
+Same bar as the plain forward (|dL| <= 1e-2 bf16 / 5e-3 fp32; |dO| within that
+plus half a bf16 ulp of O for bf16 outputs).  Rows that a window leaves without
+any visible key must come back as O = 0 exactly and L = -inf on both sides.
+Shapes span several 128-row tiles with ragged tails, windows whose edges cut
+through tiles, whole query tiles with no visible key, grouped-query heads, and
+the split-KV path with modifiers.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_helpers import TOL, compare, sample_rows, to_device, to_host_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def fa2():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_forward_fa2_gb300 as m
+    m.lib()
+    return m
+
+
+@pytest.fixture(autouse=True)
+def device_status_clean(fa2):
+    assert fa2.fa2_device_status(reset=True) == 0
+    yield
+    assert fa2.fa2_device_status(reset=True) == 0, "a kernel pipeline wait ran out"
+
+
+def alibi_slopes(B, H, per_batch):
+    """Geometric ALiBi slopes 2^(-8 (h + 1) / H); per batch entry scaled by 1/(b + 1)."""
+    base = 2.0 ** (-8.0 * np.arange(1, H + 1) / H)
+    if not per_batch:
+        return base.astype(np.float32)
+    return (base[None, :] / np.arange(1, B + 1)[:, None]).astype(np.float32)
+
+
+def check(o_gpu, l_gpu, o_ref, l_ref, dtype, what):
+    empty = np.isneginf(l_ref)
+    assert np.array_equal(np.isneginf(l_gpu), empty), f"{what}: rows without keys differ"
+    assert np.all(o_gpu[empty] == 0.0), f"{what}: O of a row without keys is not 0"
+    if np.all(empty):
+        return
+    eo, el, excess = compare(o_gpu[~empty], l_gpu[~empty], o_ref[~empty], l_ref[~empty], dtype)
+    assert excess <= 0 and el <= TOL[dtype], f"{what}: max|dO| {eo:.3g} max|dL| {el:.3g}"
+
+
+def run_case(fa2, seed, B, H, Hkv, M, N, D, dtype, causal, window, cap, slopes, num_splits=1,
+             sigma_qk=1.0, rows=None):
+    q = si.normal(seed, 1, (B, H, M, D), sigma_qk, dtype)
+    k = si.normal(seed, 2, (B, Hkv, N, D), sigma_qk, dtype)
+    v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
+    scale = 1.0 / math.sqrt(D)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    ts = torch.from_numpy(slopes).to(DEV) if slopes is not None else None
+    o, lse = fa2.fa2_fwd_ext(tq, tk, tv, scale=scale, causal=causal, window=window, softcap=cap,
+                             alibi_slopes=ts, num_splits=num_splits)
+    torch.cuda.synchronize()
+    og, lg = to_host_f64(o), lse.cpu().numpy().astype(np.float64)
+    sl = slopes.astype(np.float64) if slopes is not None else None
+    # the kernel computes in fp32 from the fp32 scale and slopes it is given
+    scale32 = float(np.float32(scale))
+    if rows is None:
+        orf, lrf = oracle.attn_fwd_mod(q, k, v, scale32, causal, window, cap, sl)
+        return og, lg, orf, lrf
+    orf, lrf = oracle.attn_fwd_mod(q, k, v, scale32, causal, window, cap, sl, rows=rows)
+    return og.reshape(-1, D)[rows], lg.reshape(-1)[rows], orf, lrf
+
+
+CASES = [  # (B, H, Hkv, M, N, D, causal, window, softcap, slopes)
+    (1, 2, 2, 300, 500, 128, False, (64, 32), 0.0, None),       # band cutting through tiles
+    (2, 2, 1, 517, 300, 64, False, (100, -1), 0.0, None),       # rows >= 400 see no key
+    (1, 2, 2, 640, 640, 128, True, (200, -1), 0.0, None),       # causal sliding window
+    (1, 1, 1, 256, 1000, 64, False, (-1, 0), 0.0, None),        # == causal
+    (1, 2, 2, 130, 700, 128, False, (0, 300), 0.0, None),       # look-ahead only
+    (2, 1, 1, 200, 150, 64, False, (0, 0), 0.0, None),          # one key per row (O = V_i)
+    (2, 2, 2, 300, 257, 128, False, (-1, -1), 3.0, None),       # softcap
+    (1, 3, 3, 333, 333, 64, True, (-1, -1), 2.0, None),         # causal softcap
+    (1, 4, 2, 400, 400, 128, True, (-1, -1), 0.0, "h"),         # ALiBi, one slope per head
+    (2, 2, 2, 200, 333, 64, False, (-1, -1), 0.0, "bh"),        # ALiBi per (b, h), both sides
+    (1, 4, 1, 390, 520, 128, True, (150, -1), 4.0, "h"),        # all three, MQA
+    (2, 2, 2, 129, 1100, 64, False, (300, 40), 2.5, "bh"),      # all three
+]
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:6])) + f"_c{int(c[6])}"
+                         + f"_w{c[7][0]}_{c[7][1]}_cap{c[8]:g}_{c[9]}")
+def test_modifiers_all_rows(fa2, case, dtype):
+    B, H, Hkv, M, N, D, causal, window, cap, sl = case
+    slopes = alibi_slopes(B, H, sl == "bh") if sl else None
+    # bf16 cases with a softcap draw larger scores (sigma 2) to reach deep into
+    # saturation; fp32 inputs stay at sigma 1, where TF32 rounding of Q and K keeps
+    # L within 5e-3 (it grows with the score magnitude)
+    sigma = 2.0 if (cap and dtype == si.BF16) else 1.0
+    og, lg, orf, lrf = run_case(fa2, 300 + CASES.index(case), B, H, Hkv, M, N, D, dtype, causal,
+                                window, cap, slopes, sigma_qk=sigma)
+    check(og, lg, orf, lrf, dtype, str(case))
+
+
+def test_one_key_window_returns_that_value_row(fa2):
+    """window (0, 0): row i sees only key i, so O_i = V_i exactly (bf16 in and out)
+    and L_i = scale q_i . k_i; rows past N see nothing."""
+    B, H, M, N, D = 1, 2, 300, 260, 128
+    og, lg, orf, lrf = run_case(fa2, 350, B, H, H, M, N, D, si.BF16, False, (0, 0), 0.0, None)
+    v = si.normal(350, 3, (B, H, N, D), 1.0, si.BF16)
+    assert np.array_equal(og[:, :, :N], si.bf16_bits_to_f32(v).astype(np.float64))
+    assert np.all(og[:, :, N:] == 0) and np.all(np.isneginf(lg[:, :, N:]))
+    check(og, lg, orf, lrf, si.BF16, "window (0, 0)")
+
+
+@pytest.mark.parametrize("num_splits", [0, 3, 7])
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+def test_modifiers_with_split_kv(fa2, num_splits, dtype):
+    """Split-KV slices with a window: some slices see no key of a row (partial
+    L = -inf) and the combine kernel must ignore them."""
+    B, H, Hkv, M, N, D = 1, 4, 2, 200, 4000, 128
+    slopes = alibi_slopes(B, H, False)
+    og, lg, orf, lrf = run_case(fa2, 360 + num_splits, B, H, Hkv, M, N, D, dtype, False, (900, 1500),
+                                3.0, slopes, num_splits=num_splits)
+    check(og, lg, orf, lrf, dtype, f"split {num_splits}")
+
+
+def test_no_modifier_matches_plain_forward_bitwise(fa2):
+    """With no modifier in use fa2_fwd_ext runs the plain kernel."""
+    B, H, M, N, D = 2, 2, 300, 400, 128
+    q, k, v = (to_device(si.normal(370, s, (B, H, M if s == 1 else N, D), 1.0, si.BF16), DEV)
+               for s in (1, 2, 3))
+    for causal in (False, True):
+        o1, l1 = fa2.fa2_fwd(q, k, v, causal=causal)
+        o2, l2 = fa2.fa2_fwd_ext(q, k, v, causal=causal, window=(-1, 5) if causal else (-1, -1))
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", [n for n, w in si.WORKLOADS.items() if w.modified])
+def test_modifier_workload_sampled_rows(fa2, name):
+    """The modifier workloads at full size (8192 x 8192, D = 128), in the call the
+    bench times, on sampled rows."""
+    w = si.WORKLOADS[name]
+    q, k, v = si.make_qkv(w)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    slopes = si.alibi_slopes(w.H) if w.alibi else None
+    ts = torch.from_numpy(slopes).to(DEV) if w.alibi else None
+    o, lse = fa2.fa2_fwd_ext(tq, tk, tv, scale=w.scale, causal=w.causal, window=w.window,
+                             softcap=w.softcap, alibi_slopes=ts, num_splits=1)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.B, w.H, w.M, w.N, w.causal, n_random=1024)
+    og = to_host_f64(o).reshape(-1, w.D)[rows]
+    lg = lse.cpu().numpy().astype(np.float64).reshape(-1)[rows]
+    orf, lrf = oracle.attn_fwd_mod(q, k, v, float(np.float32(w.scale)), w.causal, w.window, w.softcap,
+                                   slopes.astype(np.float64) if w.alibi else None, rows=rows)
+    check(og, lg, orf, lrf, w.dtype, name)
