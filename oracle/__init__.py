@@ -68,6 +68,9 @@ def _bind(lib):
     lib.oracle_attn_fwd_mod.argtypes = [vp, vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, i32, i32,
                                         dbl, i32, i32, i32, dbl, vp, i64, i32]
     lib.oracle_attn_fwd_mod.restype = i32
+    lib.oracle_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                        dbl, i32, i32]
+    lib.oracle_attn_bwd_gqa.restype = i32
     return lib
 
 
@@ -194,3 +197,24 @@ def attn_fwd_mod(q, k, v, scale: float, causal: bool, window=(-1, -1), softcap: 
     if rc:
         raise RuntimeError(f"oracle_attn_fwd_mod failed: {rc}")
     return o, lse
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool, lib=None):
+    """Gradients of the forward for upstream gradient ``dout`` (same shape and
+    dtype as q): returns (dQ [B,H,M,D], dK [B,Hkv,N,D], dV [B,Hkv,N,D]) fp64.
+    k and v may hold fewer heads than q (grouped-query attention)."""
+    lib = lib or load()
+    q, k, v, B, H, M, N, D, code = _prep(q, k, v, gqa=True)
+    dout = np.ascontiguousarray(dout)
+    if dout.shape != q.shape or dout.dtype != q.dtype:
+        raise ValueError("dout must have the shape and dtype of q")
+    Hkv = k.shape[1]
+    dq = np.empty((B, H, M, D), np.float64)
+    dk = np.empty((B, Hkv, N, D), np.float64)
+    dv = np.empty((B, Hkv, N, D), np.float64)
+    rc = lib.oracle_attn_bwd_gqa(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                 dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, B, H, Hkv, M, N, D,
+                                 float(scale), int(causal), code)
+    if rc:
+        raise RuntimeError(f"oracle_attn_bwd_gqa failed: {rc}")
+    return dq, dk, dv

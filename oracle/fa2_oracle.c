@@ -362,6 +362,98 @@ int oracle_attn_fwd_mod(const void* q, const void* k, const void* v, const int64
   return status;
 }
 
+/* ---------------------------------------------------------------------------
+ * Backward pass: the gradients of the forward above for an upstream gradient
+ * dO = dloss/dO ("From FlashAttention to FlashAttention 2", Layer 7: The Backward
+ * Kernel; "FlashAttention-2 from PyTorch to Triton", Known gaps item 5: the
+ * backward recomputes P = exp(S - L) and uses D = rowsum(dO o O)).  With
+ * P_ij = exp(s_ij - L_i) the attention weight of visible key j in row i (0 for a
+ * hidden key):
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j,   D_i = dO_i . O_i,   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij k_j,            dK_j = scale sum_i dS_ij q_i
+ * (the scale appears because s = scale q.k).  With grouped-query attention the
+ * dK and dV of a key/value head sum over the query heads that read it.  O and L
+ * are recomputed here in fp64 from q, k, v: this is the exact gradient of the
+ * exact function.  dout has the dtype of q; dq [B,H,M,D], dk and dv [B,Hkv,N,D]
+ * are fp64. */
+int oracle_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* dout, double* dq,
+                        double* dk, double* dv, int B, int H, int Hkv, int M, int N, int D,
+                        double scale, int causal, int dtype) {
+  if (check_sizes(B, H, Hkv, M, N, D, dtype)) return -1;
+  const int group = H / Hkv;
+  const int64_t kv_heads = (int64_t)B * Hkv;
+  int status = 0;
+#pragma omp parallel
+  {
+    double* p = (double*)malloc(sizeof(double) * (size_t)N);
+    double* ds = (double*)malloc(sizeof(double) * (size_t)N);
+    double* o_row = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!p || !ds || !o_row) {
+#pragma omp atomic write
+      status = -2;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t kvh = 0; kvh < kv_heads; ++kvh) {
+        const int64_t kvoff = kvh * (int64_t)N * D;
+        for (int64_t e = 0; e < (int64_t)N * D; ++e) {
+          dk[kvoff + e] = 0.0;
+          dv[kvoff + e] = 0.0;
+        }
+        for (int g = 0; g < group; ++g) {
+          const int64_t bh = (kvh / Hkv) * H + (kvh % Hkv) * group + g;
+          for (int64_t i = 0; i < M; ++i) {
+            const int64_t qoff = (bh * M + i) * (int64_t)D;
+            const int64_t nvis = visible_keys(i, N, causal);
+            /* scores, logsumexp, weights */
+            double m = -INFINITY;
+            for (int64_t j = 0; j < nvis; ++j) {
+              double dot = 0.0;
+              for (int d = 0; d < D; ++d)
+                dot += widen(q, qoff + d, dtype) * widen(k, kvoff + j * D + d, dtype);
+              p[j] = scale * dot;
+              if (p[j] > m) m = p[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) l += exp(p[j] - m);
+            const double L = m + log(l);
+            for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - L);
+            /* O_i and D_i = dO_i . O_i */
+            double Di = 0.0;
+            for (int d = 0; d < D; ++d) {
+              double acc = 0.0;
+              for (int64_t j = 0; j < nvis; ++j) acc += p[j] * widen(v, kvoff + j * D + d, dtype);
+              o_row[d] = acc;
+              Di += widen(dout, qoff + d, dtype) * acc;
+            }
+            /* dS_ij = P_ij (dO_i . v_j - D_i) */
+            for (int64_t j = 0; j < nvis; ++j) {
+              double dp = 0.0;
+              for (int d = 0; d < D; ++d)
+                dp += widen(dout, qoff + d, dtype) * widen(v, kvoff + j * D + d, dtype);
+              ds[j] = p[j] * (dp - Di);
+            }
+            for (int d = 0; d < D; ++d) {
+              double acc = 0.0;
+              for (int64_t j = 0; j < nvis; ++j) acc += ds[j] * widen(k, kvoff + j * D + d, dtype);
+              dq[qoff + d] = scale * acc;
+            }
+            for (int64_t j = 0; j < nvis; ++j)
+              for (int d = 0; d < D; ++d) {
+                dk[kvoff + j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);
+                dv[kvoff + j * D + d] += p[j] * widen(dout, qoff + d, dtype);
+              }
+          }
+        }
+      }
+    }
+    free(p);
+    free(ds);
+    free(o_row);
+  }
+  return status;
+}
+
 /* Multi-head attention: the Hkv == H case of the entry points above. */
 int oracle_attn_fwd(const void* q, const void* k, const void* v, double* o, double* lse,
                     int B, int H, int M, int N, int D, double scale, int causal, int dtype) {

@@ -370,11 +370,102 @@ def mod_closed_form_errors(lib):
     return errs
 
 
+def bwd_inputs(seed, B, H, Hkv, M, N, D, dtype=si.FP64):
+    q = si.normal(seed, 1, (B, H, M, D), 1.0, dtype)
+    k = si.normal(seed, 2, (B, Hkv, N, D), 1.0, dtype)
+    v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
+    do = si.normal(seed, 4, (B, H, M, D), 1.0, dtype)
+    return q, k, v, do
+
+
+def bwd_finite_difference_errors(lib):
+    """The backward is the gradient of f(Q, K, V) = sum(dO o O(Q, K, V)) with O
+    from the (separately pinned) forward oracle: central differences on sampled
+    elements of Q, K and V, step 1e-5, relative error <= 1e-6."""
+    errs = []
+    for n, (B, H, Hkv, M, N, D, causal) in enumerate([(1, 2, 1, 6, 9, 4, False), (2, 2, 2, 7, 5, 3, True),
+                                                       (1, 4, 2, 9, 9, 2, True)]):
+        q, k, v, do = bwd_inputs(120 + n, B, H, Hkv, M, N, D)
+        scale = 0.45
+        grads = oracle.attn_bwd(q, k, v, do, scale, causal, lib=lib)
+
+        def f(qq, kk, vv):
+            o, _ = oracle.attn_fwd_gqa(qq, kk, vv, scale, causal, lib=lib)
+            return float(np.sum(do * o))
+
+        rng = np.random.default_rng(n)
+        for which, (x, g) in enumerate(zip((q, k, v), grads)):
+            gmax = float(np.max(np.abs(g))) + 1e-300
+            for _ in range(6):
+                idx = tuple(int(rng.integers(0, s)) for s in x.shape)
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += 1e-5
+                xm[idx] -= 1e-5
+                args_p = [q, k, v]
+                args_m = [q, k, v]
+                args_p[which], args_m[which] = xp, xm
+                fd = (f(*args_p) - f(*args_m)) / 2e-5
+                if abs(fd - g[idx]) > 1e-6 * gmax:
+                    errs.append(f"bwd finite difference case {n} {'qkv'[which]}{idx}: {fd} vs {g[idx]}")
+    return errs
+
+
+def bwd_closed_form_errors(lib):
+    errs = []
+    B, H, Hkv, M, N, D = 2, 4, 2, 11, 7, 5
+    q, k, v, do = bwd_inputs(130, B, H, Hkv, M, N, D)
+    g = H // Hkv
+    for causal in (False, True):
+        # one key: O = V_0 whatever Q and K are, so dQ = dK = 0 and dV_0 = sum of dO
+        dq, dk, dv = oracle.attn_bwd(q, k[:, :, :1], v[:, :, :1], do, 0.5, causal, lib=lib)
+        want = do.reshape(B, Hkv, g, M, D).sum(axis=(2, 3))
+        if max_err(dq, 0) > 1e-14 or max_err(dk, 0) > 1e-14 or max_err(dv[:, :, 0], want) > 1e-12:
+            errs.append(f"bwd N=1 causal={causal}")
+        # K = 0: uniform weights, dV_j = sum over rows that see j of dO_i / #visible(i)
+        dq, dk, dv = oracle.attn_bwd(q, np.zeros_like(k), v, do, 0.5, causal, lib=lib)
+        nvis = np.minimum(np.arange(M) + 1, N) if causal else np.full(M, N)
+        w = np.array([[1.0 / nvis[i] if (j < nvis[i]) else 0.0 for j in range(N)] for i in range(M)])
+        want = np.einsum("ij,bkgid->bkjd", w, do.reshape(B, Hkv, g, M, D))
+        if max_err(dv, want) > 1e-12:
+            errs.append(f"bwd K=0 dV causal={causal}")
+        # rows of dS sum to zero, so the dK of every key/value head sums to zero over keys
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.5, causal, lib=lib)
+        if max_err(dk.sum(axis=2), 0) > 1e-12:
+            errs.append(f"bwd sum_j dK_j != 0 causal={causal}")
+    return errs
+
+
+def bwd_torch_errors(lib):
+    """PyTorch CPU autograd in fp64 (K/V heads repeated for grouped-query)."""
+    try:
+        import torch
+    except ImportError:
+        return []
+    errs = []
+    for n, (B, H, Hkv, M, N, D) in enumerate([(2, 4, 2, 13, 17, 8), (1, 3, 3, 20, 9, 16), (1, 2, 1, 1, 4, 4)]):
+        for dtype in (si.FP64, si.BF16):
+            q, k, v, do = bwd_inputs(140 + n, B, H, Hkv, M, N, D, dtype)
+            for causal in (False, True):
+                dq, dk, dv = oracle.attn_bwd(q, k, v, do, 0.3, causal, lib=lib)
+                tq, tk, tv = (torch.from_numpy(widen(x)).requires_grad_() for x in (q, k, v))
+                rk, rv = (t.repeat_interleave(H // Hkv, dim=1) for t in (tk, tv))
+                sc = 0.3 * tq @ rk.transpose(-1, -2)
+                if causal:
+                    sc = sc.masked_fill(~torch.ones(M, N, dtype=torch.bool).tril(), float("-inf"))
+                (torch.softmax(sc, -1) @ rv).backward(torch.from_numpy(widen(do)))
+                e = max(max_err(dq, tq.grad.numpy()), max_err(dk, tk.grad.numpy()),
+                        max_err(dv, tv.grad.numpy()))
+                if not e <= 1e-12:
+                    errs.append(f"bwd torch {(B, H, Hkv, M, N, D)} {dtype} causal={causal}: {e}")
+    return errs
+
+
 def all_pin_errors(lib):
     errs = []
     for check in (golden_errors, brute_errors, large_score_errors, invariant_errors,
                   rows_errors, tiled_errors, gqa_errors, mod_brute_errors, mod_reduction_errors,
-                  mod_closed_form_errors):
+                  mod_closed_form_errors, bwd_finite_difference_errors, bwd_closed_form_errors,
+                  bwd_torch_errors):
         try:
             errs += check(lib)
         except Exception as exc:  # a mutant may also crash or return an error code
@@ -437,6 +528,19 @@ def test_score_modifiers_reduce_to_plain_attention(oracle_lib):
 
 def test_score_modifiers_closed_forms(oracle_lib):
     assert mod_closed_form_errors(oracle_lib) == []
+
+
+def test_backward_is_the_gradient_of_the_forward(oracle_lib):
+    assert bwd_finite_difference_errors(oracle_lib) == []
+
+
+def test_backward_closed_forms(oracle_lib):
+    assert bwd_closed_form_errors(oracle_lib) == []
+
+
+def test_backward_matches_torch_autograd_fp64(oracle_lib):
+    pytest.importorskip("torch")
+    assert bwd_torch_errors(oracle_lib) == []
 
 
 def test_matches_torch_sdpa_fp64():
@@ -514,6 +618,24 @@ MUTANTS = [
     ("mod: no final divide", "o_row[d] = acc / lsum;", "o_row[d] = acc;", 1),
     ("mod: L missing max", "*lse = m + log(lsum);", "*lse = log(lsum);", 1),
     ("mod: max not subtracted", "w[j - lo] = exp(w[j - lo] - m);", "w[j - lo] = exp(w[j - lo]);", 1),
+    ("bwd: dQ scale dropped", "dq[qoff + d] = scale * acc;", "dq[qoff + d] = acc;", 1),
+    ("bwd: dK scale dropped", "dk[kvoff + j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);",
+     "dk[kvoff + j * D + d] += ds[j] * widen(q, qoff + d, dtype);", 1),
+    ("bwd: D_i added instead of subtracted", "ds[j] = p[j] * (dp - Di);", "ds[j] = p[j] * (dp + Di);", 1),
+    ("bwd: D_i dropped", "ds[j] = p[j] * (dp - Di);", "ds[j] = p[j] * dp;", 1),
+    ("bwd: dS without P", "ds[j] = p[j] * (dp - Di);", "ds[j] = dp - Di;", 1),
+    ("bwd: D_i from dO . dO", "Di += widen(dout, qoff + d, dtype) * acc;",
+     "Di += widen(dout, qoff + d, dtype) * widen(dout, qoff + d, dtype);", 1),
+    ("bwd: dV from dS", "dv[kvoff + j * D + d] += p[j] * widen(dout, qoff + d, dtype);",
+     "dv[kvoff + j * D + d] += ds[j] * widen(dout, qoff + d, dtype);", 1),
+    ("bwd: dK from K", "dk[kvoff + j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);",
+     "dk[kvoff + j * D + d] += scale * ds[j] * widen(k, kvoff + j * D + d, dtype);", 1),
+    ("bwd: P not normalised", "for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - L);",
+     "for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - m);", 1),
+    ("bwd: query heads of a group interleaved", "const int64_t bh = (kvh / Hkv) * H + (kvh % Hkv) * group + g;",
+     "const int64_t bh = (kvh / Hkv) * H + g * Hkv + (kvh % Hkv);", 1),
+    ("bwd: causal ignored", "const int64_t nvis = visible_keys(i, N, causal);\n            /* scores",
+     "const int64_t nvis = visible_keys(i, N, 0);\n            /* scores", 1),
     ("tiled: O not rescaled", "acc[(int64_t)r * D + d] = alpha * acc[(int64_t)r * D + d] + pv;",
      "acc[(int64_t)r * D + d] = acc[(int64_t)r * D + d] + pv;", 1),
     ("tiled: l not rescaled", "l_run[r] = alpha * l_run[r] + rowsum;", "l_run[r] = l_run[r] + rowsum;", 1),
