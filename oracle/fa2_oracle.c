@@ -383,73 +383,81 @@ int oracle_attn_bwd_gqa(const void* q, const void* k, const void* v, const void*
   if (check_sizes(B, H, Hkv, M, N, D, dtype)) return -1;
   const int group = H / Hkv;
   const int64_t kv_heads = (int64_t)B * Hkv;
+  const int64_t nd = (int64_t)N * D;
   int status = 0;
+  /* key/value heads one after another; the rows of a head's query heads in
+   * parallel, each thread summing its dK, dV contributions privately */
+  for (int64_t kvh = 0; kvh < kv_heads && status == 0; ++kvh) {
+    const int64_t kvoff = kvh * nd;
+    for (int64_t e = 0; e < nd; ++e) {
+      dk[kvoff + e] = 0.0;
+      dv[kvoff + e] = 0.0;
+    }
 #pragma omp parallel
-  {
-    double* p = (double*)malloc(sizeof(double) * (size_t)N);
-    double* ds = (double*)malloc(sizeof(double) * (size_t)N);
-    double* o_row = (double*)malloc(sizeof(double) * (size_t)D);
-    if (!p || !ds || !o_row) {
+    {
+      double* p = (double*)malloc(sizeof(double) * (size_t)N);
+      double* ds = (double*)malloc(sizeof(double) * (size_t)N);
+      double* dk_t = (double*)calloc((size_t)nd, sizeof(double));
+      double* dv_t = (double*)calloc((size_t)nd, sizeof(double));
+      if (!p || !ds || !dk_t || !dv_t) {
 #pragma omp atomic write
-      status = -2;
-    } else {
-#pragma omp for schedule(dynamic, 1)
-      for (int64_t kvh = 0; kvh < kv_heads; ++kvh) {
-        const int64_t kvoff = kvh * (int64_t)N * D;
-        for (int64_t e = 0; e < (int64_t)N * D; ++e) {
-          dk[kvoff + e] = 0.0;
-          dv[kvoff + e] = 0.0;
-        }
-        for (int g = 0; g < group; ++g) {
+        status = -2;
+      } else {
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < (int64_t)group * M; ++r) {
+          const int64_t g = r / M, i = r % M;
           const int64_t bh = (kvh / Hkv) * H + (kvh % Hkv) * group + g;
-          for (int64_t i = 0; i < M; ++i) {
-            const int64_t qoff = (bh * M + i) * (int64_t)D;
-            const int64_t nvis = visible_keys(i, N, causal);
-            /* scores, logsumexp, weights */
-            double m = -INFINITY;
-            for (int64_t j = 0; j < nvis; ++j) {
-              double dot = 0.0;
-              for (int d = 0; d < D; ++d)
-                dot += widen(q, qoff + d, dtype) * widen(k, kvoff + j * D + d, dtype);
-              p[j] = scale * dot;
-              if (p[j] > m) m = p[j];
-            }
-            double l = 0.0;
-            for (int64_t j = 0; j < nvis; ++j) l += exp(p[j] - m);
-            const double L = m + log(l);
-            for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - L);
-            /* O_i and D_i = dO_i . O_i */
-            double Di = 0.0;
-            for (int d = 0; d < D; ++d) {
-              double acc = 0.0;
-              for (int64_t j = 0; j < nvis; ++j) acc += p[j] * widen(v, kvoff + j * D + d, dtype);
-              o_row[d] = acc;
-              Di += widen(dout, qoff + d, dtype) * acc;
-            }
-            /* dS_ij = P_ij (dO_i . v_j - D_i) */
-            for (int64_t j = 0; j < nvis; ++j) {
-              double dp = 0.0;
-              for (int d = 0; d < D; ++d)
-                dp += widen(dout, qoff + d, dtype) * widen(v, kvoff + j * D + d, dtype);
-              ds[j] = p[j] * (dp - Di);
-            }
-            for (int d = 0; d < D; ++d) {
-              double acc = 0.0;
-              for (int64_t j = 0; j < nvis; ++j) acc += ds[j] * widen(k, kvoff + j * D + d, dtype);
-              dq[qoff + d] = scale * acc;
-            }
-            for (int64_t j = 0; j < nvis; ++j)
-              for (int d = 0; d < D; ++d) {
-                dk[kvoff + j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);
-                dv[kvoff + j * D + d] += p[j] * widen(dout, qoff + d, dtype);
-              }
+          const int64_t qoff = (bh * M + i) * (int64_t)D;
+          const int64_t nvis = visible_keys(i, N, causal);
+          /* scores, logsumexp, weights */
+          double m = -INFINITY;
+          for (int64_t j = 0; j < nvis; ++j) {
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d)
+              dot += widen(q, qoff + d, dtype) * widen(k, kvoff + j * D + d, dtype);
+            p[j] = scale * dot;
+            if (p[j] > m) m = p[j];
           }
+          double l = 0.0;
+          for (int64_t j = 0; j < nvis; ++j) l += exp(p[j] - m);
+          const double L = m + log(l);
+          for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - L);
+          /* D_i = dO_i . O_i with O_i = sum_j P_ij v_j */
+          double Di = 0.0;
+          for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) acc += p[j] * widen(v, kvoff + j * D + d, dtype);
+            Di += widen(dout, qoff + d, dtype) * acc;
+          }
+          /* dS_ij = P_ij (dO_i . v_j - D_i) */
+          for (int64_t j = 0; j < nvis; ++j) {
+            double dp = 0.0;
+            for (int d = 0; d < D; ++d)
+              dp += widen(dout, qoff + d, dtype) * widen(v, kvoff + j * D + d, dtype);
+            ds[j] = p[j] * (dp - Di);
+          }
+          for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < nvis; ++j) acc += ds[j] * widen(k, kvoff + j * D + d, dtype);
+            dq[qoff + d] = scale * acc;
+          }
+          for (int64_t j = 0; j < nvis; ++j)
+            for (int d = 0; d < D; ++d) {
+              dk_t[j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);
+              dv_t[j * D + d] += p[j] * widen(dout, qoff + d, dtype);
+            }
+        }
+#pragma omp critical
+        for (int64_t e = 0; e < nd; ++e) {
+          dk[kvoff + e] += dk_t[e];
+          dv[kvoff + e] += dv_t[e];
         }
       }
+      free(p);
+      free(ds);
+      free(dk_t);
+      free(dv_t);
     }
-    free(p);
-    free(ds);
-    free(o_row);
   }
   return status;
 }

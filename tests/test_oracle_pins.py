@@ -619,23 +619,24 @@ MUTANTS = [
     ("mod: L missing max", "*lse = m + log(lsum);", "*lse = log(lsum);", 1),
     ("mod: max not subtracted", "w[j - lo] = exp(w[j - lo] - m);", "w[j - lo] = exp(w[j - lo]);", 1),
     ("bwd: dQ scale dropped", "dq[qoff + d] = scale * acc;", "dq[qoff + d] = acc;", 1),
-    ("bwd: dK scale dropped", "dk[kvoff + j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);",
-     "dk[kvoff + j * D + d] += ds[j] * widen(q, qoff + d, dtype);", 1),
+    ("bwd: dK scale dropped", "dk_t[j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);",
+     "dk_t[j * D + d] += ds[j] * widen(q, qoff + d, dtype);", 1),
     ("bwd: D_i added instead of subtracted", "ds[j] = p[j] * (dp - Di);", "ds[j] = p[j] * (dp + Di);", 1),
     ("bwd: D_i dropped", "ds[j] = p[j] * (dp - Di);", "ds[j] = p[j] * dp;", 1),
     ("bwd: dS without P", "ds[j] = p[j] * (dp - Di);", "ds[j] = dp - Di;", 1),
     ("bwd: D_i from dO . dO", "Di += widen(dout, qoff + d, dtype) * acc;",
      "Di += widen(dout, qoff + d, dtype) * widen(dout, qoff + d, dtype);", 1),
-    ("bwd: dV from dS", "dv[kvoff + j * D + d] += p[j] * widen(dout, qoff + d, dtype);",
-     "dv[kvoff + j * D + d] += ds[j] * widen(dout, qoff + d, dtype);", 1),
-    ("bwd: dK from K", "dk[kvoff + j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);",
-     "dk[kvoff + j * D + d] += scale * ds[j] * widen(k, kvoff + j * D + d, dtype);", 1),
+    ("bwd: dV from dS", "dv_t[j * D + d] += p[j] * widen(dout, qoff + d, dtype);",
+     "dv_t[j * D + d] += ds[j] * widen(dout, qoff + d, dtype);", 1),
+    ("bwd: dK from K", "dk_t[j * D + d] += scale * ds[j] * widen(q, qoff + d, dtype);",
+     "dk_t[j * D + d] += scale * ds[j] * widen(k, kvoff + j * D + d, dtype);", 1),
+    ("bwd: thread partials of dK dropped", "dk[kvoff + e] += dk_t[e];", "dk[kvoff + e] = dk_t[e];", 1),
     ("bwd: P not normalised", "for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - L);",
      "for (int64_t j = 0; j < nvis; ++j) p[j] = exp(p[j] - m);", 1),
     ("bwd: query heads of a group interleaved", "const int64_t bh = (kvh / Hkv) * H + (kvh % Hkv) * group + g;",
      "const int64_t bh = (kvh / Hkv) * H + g * Hkv + (kvh % Hkv);", 1),
-    ("bwd: causal ignored", "const int64_t nvis = visible_keys(i, N, causal);\n            /* scores",
-     "const int64_t nvis = visible_keys(i, N, 0);\n            /* scores", 1),
+    ("bwd: causal ignored", "const int64_t nvis = visible_keys(i, N, causal);\n          /* scores",
+     "const int64_t nvis = visible_keys(i, N, 0);\n          /* scores", 1),
     ("tiled: O not rescaled", "acc[(int64_t)r * D + d] = alpha * acc[(int64_t)r * D + d] + pv;",
      "acc[(int64_t)r * D + d] = acc[(int64_t)r * D + d] + pv;", 1),
     ("tiled: l not rescaled", "l_run[r] = alpha * l_run[r] + rowsum;", "l_run[r] = l_run[r] + rowsum;", 1),
