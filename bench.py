@@ -8,6 +8,11 @@ Workload: bf16, B=2, H=16, M=N=8192, D=128, causal, scale 1/sqrt(128) (the
 configuration the >= 50%-of-peak target is stated on); FLOP = 4*B*H*M*N*D / 2.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--pass fwd|bwd]
+
+--pass bwd times the backward (fa2_bwd: dQ, dK, dV from dO, with the forward's O
+and L resident) on the same workload; its FLOP count is the usual 2.5x the
+forward's (five GEMMs of 2*M*N*D per head against the forward's two).
 
 --impl reference times the fp64 CPU oracle on the host cores (a bounded sample
 of the same workload per step): the method has no runnable reference
@@ -33,6 +38,8 @@ import seeded_inputs as si  # noqa: E402
 
 WORKLOAD = "bf16_2x16x8192x8192x128_causal"
 METRIC = "FA2 fwd TFLOP/s (4BHMND, 1/2 causal) and % of GB300 dense tensor peak"
+METRIC_BWD = "FA2 bwd TFLOP/s (10BHMND, 1/2 causal) and % of GB300 dense tensor peak"
+BWD_FLOPS_OVER_FWD = 2.5
 UNIT = "TFLOP/s"
 KERNEL = "fa2_fwd_kernel"
 def profile_summary(workload: str) -> str:
@@ -228,51 +235,86 @@ def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
     return flops / dt / 1e12, int(n), dt, cores
 
 
+def oracle_sample_bwd(w, q, k, v, seconds_target: float, seed: int = 0):
+    """Time the fp64 oracle backward on whole heads of the workload (one key/value
+    head with its query heads at a time, seeded order) until ~seconds_target.
+    Returns (TFLOP/s, heads, seconds, cores)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    group = w.H // w.Hkv
+    units = rng.permutation(w.B * w.Hkv)
+    flops_per_unit = BWD_FLOPS_OVER_FWD * w.flops / (w.B * w.Hkv)
+    dt, n = 0.0, 0
+    for u in units:
+        b, hk = divmod(int(u), w.Hkv)
+        sq = (slice(b, b + 1), slice(hk * group, (hk + 1) * group))
+        skv = (slice(b, b + 1), slice(hk, hk + 1))
+        do = si.normal(w.seed, 4, (1, group, w.M, w.D), 1.0, w.dtype)
+        t0 = time.perf_counter()
+        oracle.attn_bwd(q[sq], k[skv], v[skv], do, w.scale, w.causal)
+        dt += time.perf_counter() - t0
+        n += 1
+        if dt >= seconds_target:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    omp = os.environ.get("OMP_NUM_THREADS")
+    cores = int(omp) if omp else cores
+    return n * flops_per_unit / dt / 1e12, n * group, dt, cores
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
     w = si.WORKLOADS[args.workload]
     q, k, v = si.make_qkv(w)
+    bwd = args.pass_ == "bwd"
     per_step = []
     for step in range(args.warmup + args.steps):
-        tf, n, dt, cores = oracle_sample(w, q, k, v, seconds_target=2.0, seed=step)
+        sample = oracle_sample_bwd if bwd else oracle_sample
+        tf, n, dt, cores = sample(w, q, k, v, seconds_target=2.0, seed=step)
         if step >= args.warmup:
             per_step.append((tf, n, dt))
     value = float(np.mean([p[0] for p in per_step]))
     ms = float(np.mean([p[2] for p in per_step])) * 1e3
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M, "N": w.N,
-                   "D": w.D, "causal": w.causal},
+        "config": {"workload": w.name, "pass": args.pass_, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M,
+                   "N": w.N, "D": w.D, "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step: {per_step[-1][1]} seeded random query rows of the "
-                                   f"workload (fp64, all their visible keys), ~2 s of CPU work"},
+                         "sample": (f"per step: {per_step[-1][1]} whole query heads of the workload "
+                                    f"(fp64 backward), ~2 s of CPU work" if bwd else
+                                    f"per step: {per_step[-1][1]} seeded random query rows of the "
+                                    f"workload (fp64, all their visible keys), ~2 s of CPU work")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(args, w, q, k, v, tq, tk, tv, o, lse, step, stream, world):
-    """Same metric end to end: each step copies Q, K, V from pinned host memory,
-    runs the forward through the C ABI and copies O and L back to pinned host
+def measure_e2e(args, flops, step, stream, world, ins, outs):
+    """Same metric end to end: each step copies the step's inputs from pinned host
+    memory (``ins``: pairs of host array and its device tensor), runs the pass
+    through the C ABI and copies the results (``outs``) back to pinned host
     memory, all inside the timed region."""
     import torch
-    raw = torch.int16 if tq.dtype == torch.bfloat16 else torch.float32
-    hq, hk, hv = (torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
-                  for a in (q, k, v))
-    ho = torch.empty(o.shape, dtype=raw).pin_memory()
-    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    dq, dk, dv = tq.view(raw), tk.view(raw), tv.view(raw)
+
+    def raw(t):
+        return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+    pairs = []
+    for a, t in ins:
+        h = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+        pairs.append((h, raw(t)))
+    houts = [(torch.empty(t.shape, dtype=raw(t).dtype).pin_memory(), raw(t)) for t in outs]
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
         step()
-        ho.copy_(o.view(raw), non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+        for h, d in houts:
+            h.copy_(d, non_blocking=True)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -286,9 +328,9 @@ def measure_e2e(args, w, q, k, v, tq, tk, tv, o, lse, step, stream, world):
     e1.record(stream)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
-    return {"value": w.flops * args.steps * world / t_e2e / 1e12, "unit": UNIT,
-            "h2d_bytes_per_step": int(sum(a.nbytes for a in (q, k, v))),
-            "d2h_bytes_per_step": int(o.numel() * o.element_size() + lse.numel() * 4),
+    return {"value": flops * args.steps * world / t_e2e / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": int(sum(a.nbytes for a, _ in ins)),
+            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in outs)),
             "ms_per_step": t_e2e / args.steps * 1e3}
 
 
@@ -314,7 +356,24 @@ def run_ours(args, rank, local, world):
     stream = torch.cuda.current_stream(dev)
 
     launches_per_step = 1
-    if w.modified:
+    flops = w.flops
+    bwd = args.pass_ == "bwd"
+    e2e_ins, e2e_outs = [(q, tq), (k, tk), (v, tv)], [o, lse]
+    if bwd:
+        if w.modified or w.split_kv or w.dtype != si.BF16:
+            raise SystemExit(f"--pass bwd: workload {w.name} is not a plain bf16 one")
+        do = si.normal(w.seed, 4, q.shape, 1.0, w.dtype)
+        tdo = to_dev(do)
+        fa2.fa2_fwd(tq, tk, tv, o=o, lse=lse, scale=w.scale, causal=w.causal, stream=stream)
+        dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
+        ws = torch.empty(fa2.lib().fa2_bwd_workspace_bytes(w.B, w.H, w.M), dtype=torch.uint8, device=dev)
+        flops = BWD_FLOPS_OVER_FWD * w.flops
+        launches_per_step = 3  # preprocess, dK/dV pass, dQ pass
+
+        def step():
+            fa2.fa2_bwd(tq, tk, tv, o, lse, tdo, dq=dq, dk=dk, dv=dv, scale=w.scale, causal=w.causal,
+                        workspace=ws, stream=stream)
+    elif w.modified:
         slopes = torch.from_numpy(si.alibi_slopes(w.H)).to(dev) if w.alibi else None
 
         def step():
@@ -358,10 +417,14 @@ def run_ours(args, rank, local, world):
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     status = fa2.fa2_device_status(reset=True)
     t_total = max_over_ranks(sum(kernel_ms) / 1e3, world)
-    value = w.flops * args.steps * world / t_total / 1e12
+    value = flops * args.steps * world / t_total / 1e12
     ms_per_step = t_total / args.steps * 1e3
 
-    e2e = measure_e2e(args, w, q, k, v, tq, tk, tv, o, lse, step, stream, world) if args.e2e else None
+    if args.e2e and bwd:
+        o_host = o.view(torch.int16).cpu().numpy().view(np.uint16)
+        e2e_ins = [(q, tq), (k, tk), (v, tv), (o_host, o), (lse.cpu().numpy(), lse), (do, tdo)]
+        e2e_outs = [dq, dk, dv]
+    e2e = measure_e2e(args, flops, step, stream, world, e2e_ins, e2e_outs) if args.e2e else None
 
     if rank != 0:
         return
@@ -371,14 +434,15 @@ def run_ours(args, rank, local, world):
         # TF32 contraction: the measured bf16 peak times the nominal dense TF32/BF16 ratio
         peak = peak * TF32_OVER_BF16
         peak_kind = f"tf32 = {TF32_OVER_BF16:.3f} x {peak_kind} (nominal 1.1/2.25 PFLOP/s)"
-    achieved = w.flops / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e12
+    achieved = flops / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == si.BF16 else "tf32", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M, "N": w.N,
-                   "D": w.D, "causal": w.causal, "scale": w.scale,
+        "config": {"workload": w.name, "pass": args.pass_, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M,
+                   "N": w.N, "D": w.D, "causal": w.causal, "scale": w.scale,
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}",
                    **({"num_splits": n_split} if w.split_kv else {}),
@@ -387,8 +451,9 @@ def run_ours(args, rank, local, world):
         "frac_of_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": dram_traffic_per_launch(w.name), "kernel": KERNEL,
-                     "algorithmic_flops_per_launch": w.flops,
+                     "traffic": None if bwd else dram_traffic_per_launch(w.name),
+                     "kernel": "fa2_bwd (preprocess + dK/dV + dQ kernels)" if bwd else KERNEL,
+                     "algorithmic_flops_per_launch": flops,
                      "hbm_algorithmic_bytes_per_launch": w.io_bytes(),
                      "hbm_gbs_at_this_time": w.io_bytes() / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e9,
                      "hbm_peak_gbs": hbm_peak},
@@ -398,7 +463,12 @@ def run_ours(args, rank, local, world):
         "device_status": status,
         "wall_s_timed_region": wall,
     }
-    if args.cpu_baseline:
+    if args.cpu_baseline and bwd:
+        tf, n, dt, cores = oracle_sample_bwd(w, q, k, v, seconds_target=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"fp64 backward of {n} whole query heads of the workload "
+                                          f"in {dt:.1f} s"}
+    elif args.cpu_baseline:
         tf, n, dt, cores = oracle_sample(w, q, k, v, seconds_target=args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": f"{n} seeded random query rows of the workload (fp64, all "
@@ -414,6 +484,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(si.WORKLOADS), default=WORKLOAD,
                     help="workload to measure (default: the headline bf16 D=128 causal one)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward pass")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")

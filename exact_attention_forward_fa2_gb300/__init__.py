@@ -44,6 +44,9 @@ SIGNATURES = {
                                  _VP], _I),
     "fa2_fwd_ext": ([_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _I, _F, _VP, _I, _I,
                      _I, _VP, _SZ, _VP], _I),
+    "fa2_bwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ,
+                 _VP], _I),
+    "fa2_bwd_workspace_bytes": ([_I, _I, _I], _SZ),
     "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I], _I),
     "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "fa2_strerror": ([_I], ctypes.c_char_p),
@@ -279,6 +282,44 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool 
     if rc != FA2_OK:
         raise Fa2Error(rc, "fa2_fwd")
     return o, lse
+
+
+def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale: float | None = None,
+            causal: bool = False, workspace=None, stream=None):
+    """Backward pass (C ABI ``fa2_bwd``): gradients (dq, dk, dv) for upstream
+    gradient ``dout``, from the forward's inputs and its outputs ``o`` and
+    ``lse``.  bf16 CUDA tensors; dq like q, dk and dv like k.  The workspace is
+    allocated with torch when not given.  Returns (dq, dk, dv) without
+    synchronising."""
+    import torch
+
+    dtype = _check_qkv(q, k, v)
+    B, H, M, D = q.shape
+    H_kv, N = k.shape[1], k.shape[2]
+    for t in (o, dout):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or t.device != q.device:
+            raise ValueError("o and dout must be contiguous tensors like q")
+    if lse.shape != (B, H, M) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape [B,H,M]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, like in ((dq, q), (dk, k), (dv, v)):
+        if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous() or t.device != q.device:
+            raise ValueError("dq must be like q, dk and dv like k")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        need = lib().fa2_bwd_workspace_bytes(B, H, M)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        rc = lib().fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, M,
+                           N, D, float(scale), 1 if causal else 0, dtype, workspace.data_ptr(),
+                           workspace.numel() * workspace.element_size(), _stream_handle(q, stream))
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_bwd")
+    return dq, dk, dv
 
 
 # The grouped-query entry has the same Python signature: k and v carry H_kv heads.

@@ -11,9 +11,11 @@
 
 #include "fa2.h"
 #include "fa2_config.h"
+#include "fa2_bwd_kernel.cuh"
 #include "fa2_fwd_kernel.cuh"
 
 namespace fa2 {
+cudaError_t launch_bwd(BwdLaunch& L, int D);
 cudaError_t launch_bf16_d64(FwdLaunch& L);
 cudaError_t launch_bf16_d128(FwdLaunch& L);
 cudaError_t launch_fp32_d64(FwdLaunch& L);
@@ -79,16 +81,16 @@ int device_state(DeviceState** out) {
 }
 
 // 3-D map over a [BH, rows, D] tensor: dims (D, rows, BH) innermost first, box of
-// one 128-byte row segment x 128 rows x 1 head, 128-byte swizzle.  Rows past
+// one 128-byte row segment x box_rows rows x 1 head, 128-byte swizzle.  Rows past
 // `rows` are zero-filled on load and dropped on store, per head.
 int encode_map(CUtensorMap* map, const void* ptr, int dtype, int D, int rows, int64_t bh,
-               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, int box_rows = 128) {
   const int e = (dtype == FA2_BF16) ? 2 : 4;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                               static_cast<cuuint64_t>(bh)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * e,
                                  static_cast<cuuint64_t>(rows) * D * e};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / e), 128u, 1u};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / e), static_cast<cuuint32_t>(box_rows), 1u};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   const CUresult r = g_encode(
       map, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
@@ -225,6 +227,12 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
+// Backward workspace: L log2(e) and D = rowsum(dO o O), [B*H][M rounded up to 128] fp32 each.
+size_t bwd_workspace_bytes(int64_t bh, int M) {
+  const int64_t mpad = (static_cast<int64_t>(M) + 127) / 128 * 128;
+  return 2 * static_cast<size_t>(bh * mpad) * sizeof(float);
+}
+
 int sm_count(int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
@@ -299,20 +307,89 @@ extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, flo
   return fa2_fwd_gqa(q, k, v, o, lse, B, H, H, M, N, D, scale, causal, dtype, stream);
 }
 
+extern "C" size_t fa2_bwd_workspace_bytes(int B, int H, int M) {
+  if (B <= 0 || H <= 0 || M <= 0) return 0;
+  return bwd_workspace_bytes(static_cast<int64_t>(B) * H, M);
+}
+
+extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int M,
+                       int N, int D, float scale, int causal, int dtype, void* workspace,
+                       size_t workspace_size, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA2_ERR_NULL;
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
+  if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
+  if (D != 64 && D != 128) return FA2_ERR_HEADDIM;
+  if (dtype != FA2_BF16) return FA2_ERR_DTYPE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
+  const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+  if ((addr(q) | addr(k) | addr(v) | addr(o) | addr(dout) | addr(dq) | addr(dk) | addr(dv)) & 15u)
+    return FA2_ERR_ALIGN;
+  if (addr(lse) & 3u) return FA2_ERR_ALIGN;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  const int64_t bh_kv = static_cast<int64_t>(B) * H_kv;
+  const int64_t n_ktiles = (static_cast<int64_t>(N) + 127) / 128;
+  const int64_t n_qtiles = (static_cast<int64_t>(M) + 127) / 128;
+  if (M > (1 << 30) || N > (1 << 30) || bh * n_qtiles > INT_MAX || bh_kv * n_ktiles > INT_MAX)
+    return FA2_ERR_TOO_LARGE;
+  const size_t ws_need = bwd_workspace_bytes(bh, M);
+  if (!workspace || (addr(workspace) & 255u) || workspace_size < ws_need) return FA2_ERR_WORKSPACE;
+
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != FA2_OK) return rc;
+  fa2::BwdLaunch L;
+  rc = encode_map(&L.tmQ64, q, dtype, D, M, bh, CU_TENSOR_MAP_SWIZZLE_128B, 64);
+  if (rc == FA2_OK) rc = encode_map(&L.tmdO64, dout, dtype, D, M, bh, CU_TENSOR_MAP_SWIZZLE_128B, 64);
+  if (rc == FA2_OK) rc = encode_map(&L.tmK128, k, dtype, D, N, bh_kv);
+  if (rc == FA2_OK) rc = encode_map(&L.tmV128, v, dtype, D, N, bh_kv);
+  if (rc == FA2_OK) rc = encode_map(&L.tmdK, dk, dtype, D, N, bh_kv);
+  if (rc == FA2_OK) rc = encode_map(&L.tmdV, dv, dtype, D, N, bh_kv);
+  if (rc == FA2_OK) rc = encode_map(&L.tmQ128, q, dtype, D, M, bh);
+  if (rc == FA2_OK) rc = encode_map(&L.tmdO128, dout, dtype, D, M, bh);
+  if (rc == FA2_OK) rc = encode_map(&L.tmK64, k, dtype, D, N, bh_kv, CU_TENSOR_MAP_SWIZZLE_128B, 64);
+  if (rc == FA2_OK) rc = encode_map(&L.tmV64, v, dtype, D, N, bh_kv, CU_TENSOR_MAP_SWIZZLE_128B, 64);
+  if (rc == FA2_OK) rc = encode_map(&L.tmdQ, dq, dtype, D, M, bh);
+  if (rc != FA2_OK) return rc;
+  const int64_t mpad = n_qtiles * 128;
+  L.lse2 = static_cast<float*>(workspace);
+  L.dlt = L.lse2 + bh * mpad;
+  L.params.lse2 = L.lse2;
+  L.params.dlt = L.dlt;
+  L.params.status = st->status;
+  L.params.M = M;
+  L.params.N = N;
+  L.params.Mpad = static_cast<int>(mpad);
+  L.params.H = H;
+  L.params.group = H / H_kv;
+  L.params.BH = static_cast<int>(bh);
+  L.params.BHkv = static_cast<int>(bh_kv);
+  L.params.n_ktiles = static_cast<int>(n_ktiles);
+  L.params.n_qtiles = static_cast<int>(n_qtiles);
+  L.params.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  L.params.scale = scale;
+  L.o = o;
+  L.dout = dout;
+  L.lse = lse;
+  L.causal = causal ? 1 : 0;
+  L.stream = static_cast<cudaStream_t>(stream);
+  return fa2::launch_bwd(L, D) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
 extern "C" const char* fa2_strerror(int status) {
   switch (status) {
     case FA2_OK: return "ok";
     case FA2_ERR_NULL: return "a required pointer is NULL";
     case FA2_ERR_SHAPE: return "B, H, M, N and H_kv must be positive and H_kv must divide H";
     case FA2_ERR_HEADDIM: return "head dimension D must be 64 or 128";
-    case FA2_ERR_DTYPE: return "dtype must be FA2_BF16 or FA2_FP32";
+    case FA2_ERR_DTYPE: return "dtype must be FA2_BF16 or FA2_FP32 (FA2_BF16 for the backward)";
     case FA2_ERR_ALIGN: return "q, k, v, o must be 16-byte aligned and lse 4-byte aligned";
     case FA2_ERR_SCALE: return "scale must be finite and positive";
     case FA2_ERR_TOO_LARGE: return "sizes exceed the grid or tensor-map limits";
     case FA2_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103)";
     case FA2_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case FA2_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait ran out of time";
-    case FA2_ERR_WORKSPACE: return "split-KV workspace missing, not 256-byte aligned or too small";
+    case FA2_ERR_WORKSPACE: return "workspace missing, not 256-byte aligned or too small";
     case FA2_ERR_MODIFIER: return "softcap must be finite and >= 0, alibi_batch_stride 0 or H";
     default: return "unknown status";
   }

@@ -1,0 +1,69 @@
+// Instantiation and launch of the backward kernels (bf16, head dim 64 and 128):
+// preprocess, then the dK/dV pass, then the dQ pass, all on the caller's stream.
+#include "fa2_bwd_kernel.cuh"
+
+namespace fa2 {
+
+namespace {
+
+template <class C, bool kCausal>
+cudaError_t launch_dkdv(BwdLaunch& L, bool& attr_done) {
+  using Lay = DkvLayout<C>;
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<C, kCausal>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const dim3 grid(static_cast<unsigned>(L.params.BHkv * L.params.n_ktiles));
+  bwd_dkdv_kernel<C, kCausal><<<grid, C::kThreads, Lay::kSmemBytes, L.stream>>>(
+      L.tmQ64, L.tmdO64, L.tmK128, L.tmV128, L.tmdK, L.tmdV, L.params);
+  return cudaGetLastError();
+}
+
+template <class C, bool kCausal>
+cudaError_t launch_dq(BwdLaunch& L, bool& attr_done) {
+  using Lay = DqLayout<C>;
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<C, kCausal>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const dim3 grid(static_cast<unsigned>(L.params.BH * L.params.n_qtiles));
+  bwd_dq_kernel<C, kCausal><<<grid, C::kThreads, Lay::kSmemBytes, L.stream>>>(L.tmQ128, L.tmdO128, L.tmK64,
+                                                                             L.tmV64, L.tmdQ, L.params);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
+  using C = BwdCfg<D, D == 64 ? 8 : 4>;  // deeper ring at D = 64 (keeps one CTA per SM)
+  static bool attr[64][4] = {};
+  const int64_t rows_pad = static_cast<int64_t>(L.params.BH) * L.params.Mpad;
+  const int64_t need = (rows_pad + 7) / 8;
+  const int blocks = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
+  bwd_preprocess_kernel<D><<<blocks, 256, 0, L.stream>>>(
+      static_cast<const __nv_bfloat16*>(L.o), static_cast<const __nv_bfloat16*>(L.dout), L.lse, L.lse2, L.dlt,
+      L.params.M, L.params.Mpad, rows_pad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  bool* a = attr[dev];
+  e = L.causal ? launch_dkdv<C, true>(L, a[1]) : launch_dkdv<C, false>(L, a[0]);
+  if (e != cudaSuccess) return e;
+  return L.causal ? launch_dq<C, true>(L, a[3]) : launch_dq<C, false>(L, a[2]);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(BwdLaunch& L, int D) {
+  int dev = 0, sms = 148;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  return D == 64 ? launch_all<64>(L, dev, sms) : launch_all<128>(L, dev, sms);
+}
+
+}  // namespace fa2

@@ -1,0 +1,712 @@
+// FlashAttention-2 backward kernels for sm_103a (GB300), bf16 inputs.
+//
+// What they compute ("From FlashAttention to FlashAttention 2", Backward Pass:
+// Recomputation and Layer 7: The Backward Kernel; "FlashAttention-2 from PyTorch
+// to Triton", Known gaps item 5): for upstream gradient dO, with the forward's
+// stored logsumexp L and output O,
+//   P_ij  = exp(scale q_i.k_j - L_i)           (recomputed tile by tile, 0 if hidden)
+//   D_i   = rowsum(dO_i o O_i)
+//   dS_ij = P_ij (dO_i.v_j - D_i)
+//   dV_j  = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
+// The N x N matrices P and dS exist only tile by tile, in TMEM.
+//
+// Three launches:
+//   bwd_preprocess    D_i and L_i log2(e) per query row into a padded workspace
+//                     (rows past M get D = 0 and L = +inf, so their P is 0)
+//   bwd_dkdv_kernel   one CTA per (batch, key/value head, 128-key tile): the pages'
+//                     K/V-outer loop.  It streams 64-row tiles of Q and dO (over
+//                     every query head of the group) and accumulates dV and dK
+//                     in TMEM with four tcgen05 GEMMs per step:
+//                       S^T = K Q^T, dP^T = V dO^T   (keys on TMEM lanes)
+//                       dV += P^T dO, dK += dS^T Q   (P^T, dS^T read from TMEM)
+//   bwd_dq_kernel     one CTA per (batch, head, 128-query tile): the second pass
+//                     the pages allow for dQ instead of atomics.  It streams
+//                     64-row tiles of K and V: S = Q K^T, dP = dO V^T, dQ += dS K.
+// Both GEMM kernels recompute S and dP; dQ needs no atomics, so the result is
+// bitwise reproducible.
+//
+// Warp roles per CTA: warps 0-3 compute P and dS (thread r owns TMEM lane r),
+// warp 4 issues every tcgen05.mma from one thread, warp 5 issues the TMA copies.
+// TMEM: two stages of {S or S^T: 64 columns, dP or dP^T: 64 columns} so the
+// tensor core computes step t+1 while the CUDA cores work on step t, then the
+// fp32 accumulators (dV and dK, or dQ).  Every mbarrier wait is bounded in time
+// and winds the CTA down like the forward kernel.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fa2_fwd_kernel.cuh"
+
+namespace fa2 {
+
+struct BwdParams {
+  const float* lse2;  // [BH][Mpad]: L * log2(e); rows >= M: +inf
+  const float* dlt;   // [BH][Mpad]: rowsum(dO o O); rows >= M: 0
+  int* status;        // sticky device status word
+  int M, N, Mpad;     // Mpad = M rounded up to 128
+  int H, group;       // query heads per batch entry; query heads per key/value head
+  int BH, BHkv;       // B * H, B * H_kv
+  int n_ktiles;       // ceil(N / 128): key tiles per key/value head
+  int n_qtiles;       // ceil(M / 128): query tiles per head
+  float scale_log2;   // scale * log2(e)
+  float scale;        // dK and dQ carry one factor of scale
+};
+
+enum : int {
+  kStatusBwdTimeoutTma = 20,
+  kStatusBwdTimeoutMmaLoad = 21,
+  kStatusBwdTimeoutMmaP = 22,
+  kStatusBwdTimeoutSoftmax = 23,
+  kStatusBwdTimeoutEpilogue = 24,
+};
+
+// ------------------------------------------------------------------ preprocess
+// One warp per query row: D_i = sum_d dO[i,d] O[i,d] in fp32 from bf16, and
+// L_i log2(e).  Rows in [M, Mpad) of every head get D = 0, L = +inf.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                             const __nv_bfloat16* __restrict__ dout,
+                                                             const float* __restrict__ lse,
+                                                             float* __restrict__ lse2,
+                                                             float* __restrict__ dlt, int M, int Mpad,
+                                                             int64_t rows_pad) {
+  constexpr int kPer = D / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows_pad;
+       r += warps) {
+    const int64_t bh = r / Mpad;
+    const int i = static_cast<int>(r % Mpad);
+    float acc = 0.f;
+    if (i < M) {
+      const int64_t off = (bh * M + i) * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + off + e);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dout + off + e);
+        acc = fmaf(__low2float(a), __low2float(b), acc);
+        acc = fmaf(__high2float(a), __high2float(b), acc);
+      }
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (lane == 0) {
+      dlt[r] = acc;
+      lse2[r] = i < M ? lse[bh * M + i] * 1.4426950408889634f : INFINITY;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ shared configuration
+template <int D_, int kStages_>
+struct BwdCfg {
+  static constexpr int D = D_;
+  static constexpr int kStages = kStages_;  // depth of the ring of streamed tiles
+  static constexpr int BF = 128;            // rows of the fixed tile (keys or queries)
+  static constexpr int BS = 64;             // rows of a streamed tile per step
+  static constexpr int kColBlocks = D / 64;  // 128-byte column blocks of a bf16 row
+  static constexpr int kFixBlock = BF * 128;  // one column block of a 128-row tile
+  static constexpr int kStrBlock = BS * 128;  // one column block of a 64-row tile
+  static constexpr int kFixTile = kColBlocks * kFixBlock;
+  static constexpr int kStrTile = kColBlocks * kStrBlock;
+  static constexpr int kMmaK = 16;  // bf16 elements per MMA K step (32 bytes)
+  static constexpr int kStepsD = D / kMmaK;
+  static constexpr int kThreads = 192;
+  static constexpr int kMmaWarp = 4;
+  static constexpr int kTmaWarp = 5;
+  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: stage s holds S (or S^T) at [128 s, +64) and dP (or dP^T) at
+  // [128 s + 64, +64); P and dS overwrite them as packed bf16 (32 columns each)
+  __host__ __device__ static constexpr int kColS(int s) { return 128 * s; }
+  __host__ __device__ static constexpr int kColDP(int s) { return 128 * s + 64; }
+  static constexpr int kColAcc0 = 256;      // dV (dK/dV kernel) or dQ (dQ kernel)
+  static constexpr int kColAcc1 = 256 + D;  // dK (dK/dV kernel)
+  static constexpr uint32_t kIdescS = ptx::make_idesc(true, false, BF, BS);  // B K-major, N = 64
+  static constexpr uint32_t kIdescAcc = ptx::make_idesc(true, true, BF, D);  // B MN-major, N = D
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kColAcc1 + D <= 512, "TMEM budget");
+};
+
+// Bounded waits shared by the roles; `ok` turns false on abort or timeout.
+#define FA2_BWD_WAIT(bar_addr, parity, code) wait_bounded((bar_addr), (parity), wctx, (code))
+
+// ------------------------------------------------------------------ dK, dV
+template <class C>
+struct DkvLayout {
+  // shared memory: K, V (fixed, 128 rows), then kStages x {Q, dO (64 rows), L2, D vectors}
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + C::kFixTile;
+  static constexpr int kOffRing = kOffV + C::kFixTile;
+  // (a stage starts on a 1024-byte boundary, as the 128-byte swizzle requires)
+  static constexpr int kStageBytes = (2 * C::kStrTile + 2 * C::BS * 4 + 1023) / 1024 * 1024;
+  static constexpr int kOffBar = kOffRing + C::kStages * kStageBytes;
+  // barriers: KV, full[S], empty[S], sfull[2], pfull[2], done
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = kBarFull + C::kStages;
+  static constexpr int kBarSFull = kBarEmpty + C::kStages;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarDone = kBarPFull + 2;
+  static constexpr int kNumBars = kBarDone + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  __host__ __device__ static constexpr int q_off(int s) { return kOffRing + s * kStageBytes; }
+  __host__ __device__ static constexpr int do_off(int s) { return q_off(s) + C::kStrTile; }
+  __host__ __device__ static constexpr int l2_off(int s) { return q_off(s) + 2 * C::kStrTile; }
+  __host__ __device__ static constexpr int dl_off(int s) { return l2_off(s) + C::BS * 4; }
+};
+
+// Work of one dK/dV CTA: query steps of 64 rows over every head of the group.
+struct DkvUnit {
+  int bhkv;   // flat batch * H_kv + key/value head
+  int jt;     // key tile
+  int i0;     // first 64-row query step that sees a key of this tile
+  int nq;     // steps per query head
+  int steps;  // group * nq
+};
+
+template <bool kCausal>
+__device__ __forceinline__ DkvUnit dkv_unit(const BwdParams& p, int b) {
+  DkvUnit u;
+  if (kCausal) {  // smallest key tile first: it has the most query steps
+    u.jt = b / p.BHkv;
+    u.bhkv = b % p.BHkv;
+  } else {  // tiles of one key/value head adjacent: Q and dO of its heads stay in L2
+    u.bhkv = b / p.n_ktiles;
+    u.jt = b % p.n_ktiles;
+  }
+  const int nsteps = (p.M + 63) / 64;
+  u.i0 = kCausal ? min(u.jt * 2, nsteps) : 0;  // queries below the tile's first key see none of it
+  u.nq = nsteps - u.i0;
+  u.steps = u.nq * p.group;
+  return u;
+}
+
+template <class C, bool kCausal>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                    const BwdParams p) {
+  using namespace ptx;
+  using Lay = DkvLayout<C>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + Lay::kOffMisc);
+  const int warp = static_cast<int>(threadIdx.x) / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+  auto bar = [&](int i) -> uint32_t { return base + Lay::kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  const DkvUnit u = dkv_unit<kCausal>(p, static_cast<int>(blockIdx.x));
+  const int key0 = u.jt * C::BF;
+  const int Hkv = p.H / p.group;
+  // query head of step t and its first row
+  auto step_head = [&](int t) { return (u.bhkv / Hkv) * p.H + (u.bhkv % Hkv) * p.group + t / u.nq; };
+  auto step_row0 = [&](int t) { return (u.i0 + t % u.nq) * C::BS; };
+
+  if (threadIdx.x == 0) {
+    misc[1] = 0u;
+    misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
+    mbar_init(bar(Lay::kBarKV), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(Lay::kBarFull + s), 1);
+      mbar_init(bar(Lay::kBarEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Lay::kBarSFull + s), 1);
+      mbar_init(bar(Lay::kBarPFull + s), 128);
+    }
+    mbar_init(bar(Lay::kBarDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kTmaWarp && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmdO);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(base + Lay::kOffMisc, C::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = misc[0];
+  const bool skip = misc[2] != 0u;
+  const WaitCtx wctx{misc + 1, p.status};
+
+  if (!skip && warp == C::kTmaWarp) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_fix = l2_policy_evict_first();
+      const uint64_t pol_str = l2_policy_evict_last();
+      mbar_arrive_expect_tx(bar(Lay::kBarKV), 2 * C::kFixTile);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb) {
+        tma_load_3d_hint(base + Lay::kOffK + cb * C::kFixBlock, &tmK, bar(Lay::kBarKV), cb * 64, key0,
+                         u.bhkv, pol_fix);
+        tma_load_3d_hint(base + Lay::kOffV + cb * C::kFixBlock, &tmV, bar(Lay::kBarKV), cb * 64, key0,
+                         u.bhkv, pol_fix);
+      }
+      int issued = 0;
+      for (int t = 0; t < u.steps; ++t) {
+        const int s = t % C::kStages;
+        const uint32_t use = static_cast<uint32_t>(t / C::kStages);
+        if (use > 0 && !FA2_BWD_WAIT(bar(Lay::kBarEmpty + s), (use - 1) & 1u, kStatusBwdTimeoutTma)) break;
+        const int bh = step_head(t), row0 = step_row0(t);
+        const uint32_t fb = bar(Lay::kBarFull + s);
+        mbar_arrive_expect_tx(fb, 2 * C::kStrTile + 2 * C::BS * 4);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb) {
+          tma_load_3d_hint(base + Lay::q_off(s) + cb * C::kStrBlock, &tmQ, fb, cb * 64, row0, bh, pol_str);
+          tma_load_3d_hint(base + Lay::do_off(s) + cb * C::kStrBlock, &tmdO, fb, cb * 64, row0, bh, pol_str);
+        }
+        const int64_t vec = static_cast<int64_t>(bh) * p.Mpad + row0;
+        bulk_load_1d(base + Lay::l2_off(s), p.lse2 + vec, C::BS * 4, fb);
+        bulk_load_1d(base + Lay::dl_off(s), p.dlt + vec, C::BS * 4, fb);
+        issued = t + 1;
+      }
+      if (*wctx.abort_flag) {
+        drain_bounded(bar(Lay::kBarKV), 0);
+        for (int t = max(0, issued - C::kStages); t < issued; ++t)
+          drain_bounded(bar(Lay::kBarFull + t % C::kStages), (t / C::kStages) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (!skip && warp == C::kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = FA2_BWD_WAIT(bar(Lay::kBarKV), 0, kStatusBwdTimeoutMmaLoad);
+      for (int t = 0; ok && t <= u.steps; ++t) {
+        if (t < u.steps) {
+          const int s = t % C::kStages, ts = t % 2;
+          ok = FA2_BWD_WAIT(bar(Lay::kBarFull + s), (t / C::kStages) & 1, kStatusBwdTimeoutMmaLoad);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 64 queries, K = D
+#pragma unroll
+          for (int kk = 0; kk < C::kStepsD; ++kk) {
+            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
+            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
+            mma_f16_ss(tmem + C::kColS(ts), smem_desc_sw128(base + Lay::kOffK + fo, 16, 1024),
+                       smem_desc_sw128(base + Lay::q_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::kStepsD; ++kk) {
+            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
+            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
+            mma_f16_ss(tmem + C::kColDP(ts), smem_desc_sw128(base + Lay::kOffV + fo, 16, 1024),
+                       smem_desc_sw128(base + Lay::do_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::kBarSFull + ts));
+        }
+        if (t >= 1) {
+          const int tp = t - 1, sp = tp % C::kStages, tsp = tp % 2;
+          ok = FA2_BWD_WAIT(bar(Lay::kBarPFull + tsp), (tp / 2) & 1, kStatusBwdTimeoutMmaP);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, K = 64 queries;
+          // A from TMEM (packed bf16), B = the 64-row tile read MN-major
+#pragma unroll
+          for (int kk = 0; kk < C::BS / C::kMmaK; ++kk) {
+            const uint32_t bo = kk * C::kMmaK * 128;
+            mma_f16_ts(tmem + C::kColAcc0, tmem + C::kColS(tsp) + kk * 8,
+                       smem_desc(base + Lay::do_off(sp) + bo, C::kStrBlock, 1024, kLayoutSw128), C::kIdescAcc,
+                       (tp > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ts(tmem + C::kColAcc1, tmem + C::kColDP(tsp) + kk * 8,
+                       smem_desc(base + Lay::q_off(sp) + bo, C::kStrBlock, 1024, kLayoutSw128), C::kIdescAcc,
+                       (tp > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::kBarEmpty + sp));
+        }
+      }
+      tc_commit(bar(Lay::kBarDone));
+      drain_bounded(bar(Lay::kBarDone), 0);
+    }
+    __syncwarp();
+  } else if (!skip && warp < 4) {
+    // ---------------------------------------------------------- P and dS
+    const int r = warp * 32 + lane;  // key row of the tile = TMEM lane
+    const int key = key0 + r;
+    const bool key_ok = key < p.N;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < u.steps; ++t) {
+      const int s = t % C::kStages, ts = t % 2;
+      // S^T and dP^T of this step are in TMEM; the L and D vectors of the step
+      // were copied by TMA with the stage (wait on both)
+      ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarSFull + ts), (t / 2) & 1, kStatusBwdTimeoutSoftmax));
+      if (ok)
+        ok = __all_sync(0xffffffffu,
+                        FA2_BWD_WAIT(bar(Lay::kBarFull + s), (t / C::kStages) & 1, kStatusBwdTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t sv[64], dv[64];
+      tmem_ld_x32(tmem + lane_addr + C::kColS(ts), *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColS(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts), *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      tmem_ld_wait();
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      const int row0 = step_row0(t);
+      // causal: query row0 + c sees this key iff row0 + c >= key (diagonal steps only)
+      const int lim = (kCausal && row0 < key0 + C::BF) ? key - row0 : -1;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c4 = 0; c4 < C::BS; c4 += 4) {
+        float l2[4], dl[4];
+        ld_shared_v4(base + Lay::l2_off(s) + c4 * 4, l2[0], l2[1], l2[2], l2[3]);
+        ld_shared_v4(base + Lay::dl_off(s) + c4 * 4, dl[0], dl[1], dl[2], dl[3]);
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = c4 + e;
+          const bool vis = key_ok && c >= lim;
+          const float pe = vis ? ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l2[e])) : 0.f;
+          pv[e] = pe;
+          dsv[e] = pe * (__uint_as_float(dv[c]) - dl[e]);
+        }
+        pk[c4 / 2] = pack_bf16x2(pv[0], pv[1]);
+        pk[c4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+        dk[c4 / 2] = pack_bf16x2(dsv[0], dsv[1]);
+        dk[c4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+      }
+      tmem_st_x32(tmem + lane_addr + C::kColS(ts), pk);
+      tmem_st_x32(tmem + lane_addr + C::kColDP(ts), dk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(Lay::kBarPFull + ts));
+    }
+    // ------------------------------------------------------------ epilogue
+    // dV and scale * dK of this key row -> bf16 -> swizzled staging in the V and
+    // K tiles (free once every MMA has completed) -> TMA store, clipped at N
+    if (ok)
+      ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarDone), 0, kStatusBwdTimeoutEpilogue));
+    if (ok) {
+      tc_fence_after_sync();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t stage = base + (which == 0 ? Lay::kOffV : Lay::kOffK);
+        const float mul = which == 0 ? 1.0f : p.scale;
+#pragma unroll
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+          uint32_t v[32];
+          if (u.steps > 0) {
+            tmem_ld_x32(tmem + lane_addr + (which == 0 ? C::kColAcc0 : C::kColAcc1) + ch * 32, v);
+            tmem_ld_wait();
+            reg_fence_x32(v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;  // no query sees these keys: zero gradients
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int cidx = ch * 4 + q4;
+            const int cb = cidx / 8, c = cidx % 8;
+            const uint32_t addr = stage + cb * C::kFixBlock + r * 128 + ((c ^ (r & 7)) << 4);
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * mul, __uint_as_float(v[q4 * 8 + 2 * e + 1]) * mul);
+            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (r == 0 && ok && *wctx.abort_flag == 0u) {
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb) {
+        tma_store_3d(&tmdV, base + Lay::kOffV + cb * C::kFixBlock, cb * 64, key0, u.bhkv);
+        tma_store_3d(&tmdK, base + Lay::kOffK + cb * C::kFixBlock, cb * 64, key0, u.bhkv);
+      }
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+template <class C>
+struct DqLayout {
+  // shared memory: Q, dO (fixed, 128 rows), then kStages x {K, V (64 rows)}
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kOffQ + C::kFixTile;
+  static constexpr int kOffRing = kOffDO + C::kFixTile;
+  static constexpr int kStageBytes = 2 * C::kStrTile;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static constexpr int kOffBar = kOffRing + C::kStages * kStageBytes;
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = kBarFull + C::kStages;
+  static constexpr int kBarSFull = kBarEmpty + C::kStages;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarDone = kBarPFull + 2;
+  static constexpr int kNumBars = kBarDone + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  __host__ __device__ static constexpr int k_off(int s) { return kOffRing + s * kStageBytes; }
+  __host__ __device__ static constexpr int v_off(int s) { return k_off(s) + C::kStrTile; }
+};
+
+template <class C, bool kCausal>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
+  using namespace ptx;
+  using Lay = DqLayout<C>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + Lay::kOffMisc);
+  const int warp = static_cast<int>(threadIdx.x) / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+  auto bar = [&](int i) -> uint32_t { return base + Lay::kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  // unit: causal tiles longest first (largest query tile), else one head's tiles adjacent
+  const int b = static_cast<int>(blockIdx.x);
+  int bh, qt;
+  if (kCausal) {
+    qt = p.n_qtiles - 1 - b / p.BH;
+    bh = b % p.BH;
+  } else {
+    bh = b / p.n_qtiles;
+    qt = b % p.n_qtiles;
+  }
+  const int row0 = qt * C::BF;
+  const int bh_kv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
+  const int last_row = min(row0 + C::BF, p.M) - 1;
+  const int key_end = kCausal ? min(p.N, last_row + 1) : p.N;  // keys [0, key_end) are visible to some row
+  const int steps = (key_end + C::BS - 1) / C::BS;
+
+  if (threadIdx.x == 0) {
+    misc[1] = 0u;
+    misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
+    mbar_init(bar(Lay::kBarQ), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(Lay::kBarFull + s), 1);
+      mbar_init(bar(Lay::kBarEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(Lay::kBarSFull + s), 1);
+      mbar_init(bar(Lay::kBarPFull + s), 128);
+    }
+    mbar_init(bar(Lay::kBarDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kTmaWarp && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmdO);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(base + Lay::kOffMisc, C::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = misc[0];
+  const bool skip = misc[2] != 0u;
+  const WaitCtx wctx{misc + 1, p.status};
+
+  if (!skip && warp == C::kTmaWarp) {
+    if (lane == 0) {
+      const uint64_t pol_fix = l2_policy_evict_first();
+      const uint64_t pol_str = l2_policy_evict_last();
+      mbar_arrive_expect_tx(bar(Lay::kBarQ), 2 * C::kFixTile);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb) {
+        tma_load_3d_hint(base + Lay::kOffQ + cb * C::kFixBlock, &tmQ, bar(Lay::kBarQ), cb * 64, row0, bh, pol_fix);
+        tma_load_3d_hint(base + Lay::kOffDO + cb * C::kFixBlock, &tmdO, bar(Lay::kBarQ), cb * 64, row0, bh,
+                         pol_fix);
+      }
+      int issued = 0;
+      for (int t = 0; t < steps; ++t) {
+        const int s = t % C::kStages;
+        const uint32_t use = static_cast<uint32_t>(t / C::kStages);
+        if (use > 0 && !FA2_BWD_WAIT(bar(Lay::kBarEmpty + s), (use - 1) & 1u, kStatusBwdTimeoutTma)) break;
+        const uint32_t fb = bar(Lay::kBarFull + s);
+        mbar_arrive_expect_tx(fb, 2 * C::kStrTile);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb) {
+          tma_load_3d_hint(base + Lay::k_off(s) + cb * C::kStrBlock, &tmK, fb, cb * 64, t * C::BS, bh_kv, pol_str);
+          tma_load_3d_hint(base + Lay::v_off(s) + cb * C::kStrBlock, &tmV, fb, cb * 64, t * C::BS, bh_kv, pol_str);
+        }
+        issued = t + 1;
+      }
+      if (*wctx.abort_flag) {
+        drain_bounded(bar(Lay::kBarQ), 0);
+        for (int t = max(0, issued - C::kStages); t < issued; ++t)
+          drain_bounded(bar(Lay::kBarFull + t % C::kStages), (t / C::kStages) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (!skip && warp == C::kMmaWarp) {
+    if (lane == 0) {
+      bool ok = FA2_BWD_WAIT(bar(Lay::kBarQ), 0, kStatusBwdTimeoutMmaLoad);
+      for (int t = 0; ok && t <= steps; ++t) {
+        if (t < steps) {
+          const int s = t % C::kStages, ts = t % 2;
+          ok = FA2_BWD_WAIT(bar(Lay::kBarFull + s), (t / C::kStages) & 1, kStatusBwdTimeoutMmaLoad);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // S = Q K^T and dP = dO V^T: M = 128 queries, N = 64 keys, K = D
+#pragma unroll
+          for (int kk = 0; kk < C::kStepsD; ++kk) {
+            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
+            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
+            mma_f16_ss(tmem + C::kColS(ts), smem_desc_sw128(base + Lay::kOffQ + fo, 16, 1024),
+                       smem_desc_sw128(base + Lay::k_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < C::kStepsD; ++kk) {
+            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
+            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
+            mma_f16_ss(tmem + C::kColDP(ts), smem_desc_sw128(base + Lay::kOffDO + fo, 16, 1024),
+                       smem_desc_sw128(base + Lay::v_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(Lay::kBarSFull + ts));
+        }
+        if (t >= 1) {
+          const int tp = t - 1, sp = tp % C::kStages, tsp = tp % 2;
+          ok = FA2_BWD_WAIT(bar(Lay::kBarPFull + tsp), (tp / 2) & 1, kStatusBwdTimeoutMmaP);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // dQ += dS K: M = 128 queries, N = D, K = 64 keys; dS from TMEM, K tile MN-major
+#pragma unroll
+          for (int kk = 0; kk < C::BS / C::kMmaK; ++kk)
+            mma_f16_ts(tmem + C::kColAcc0, tmem + C::kColS(tsp) + kk * 8,
+                       smem_desc(base + Lay::k_off(sp) + kk * C::kMmaK * 128, C::kStrBlock, 1024, kLayoutSw128),
+                       C::kIdescAcc, (tp > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(Lay::kBarEmpty + sp));
+        }
+      }
+      tc_commit(bar(Lay::kBarDone));
+      drain_bounded(bar(Lay::kBarDone), 0);
+    }
+    __syncwarp();
+  } else if (!skip && warp < 4) {
+    const int r = warp * 32 + lane;  // query row of the tile = TMEM lane
+    const int row = row0 + r;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const int64_t vec = static_cast<int64_t>(bh) * p.Mpad + row;  // row < Mpad always
+    const float l2 = p.lse2[vec];
+    const float dl = p.dlt[vec];
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < steps; ++t) {
+      const int ts = t % 2;
+      ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarSFull + ts), (t / 2) & 1, kStatusBwdTimeoutSoftmax));
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t sv[64], dv[64];
+      tmem_ld_x32(tmem + lane_addr + C::kColS(ts), *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColS(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts), *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      tmem_ld_wait();
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      // keys past N (zero-filled rows of K) and, when causal, keys after this row
+      const int kbase = t * C::BS;
+      int lim = p.N - 1 - kbase;
+      if (kCausal) lim = min(lim, row - kbase);
+      uint32_t dk[32];
+#pragma unroll
+      for (int c = 0; c < C::BS; c += 2) {
+        float d2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pe = (c + e <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[c + e]), sl2, -l2)) : 0.f;
+          d2[e] = pe * (__uint_as_float(dv[c + e]) - dl);
+        }
+        dk[c / 2] = pack_bf16x2(d2[0], d2[1]);
+      }
+      tmem_st_x32(tmem + lane_addr + C::kColS(ts), dk);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(Lay::kBarPFull + ts));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarDone), 0, kStatusBwdTimeoutEpilogue));
+    if (ok) {
+      tc_fence_after_sync();
+      const uint32_t stage = base + Lay::kOffQ;  // Q's tile is free once every MMA has completed
+#pragma unroll
+      for (int ch = 0; ch < C::D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_addr + C::kColAcc0 + ch * 32, v);
+        tmem_ld_wait();
+        reg_fence_x32(v);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int cidx = ch * 4 + q4;
+          const int cb = cidx / 8, c = cidx % 8;
+          const uint32_t addr = stage + cb * C::kFixBlock + r * 128 + ((c ^ (r & 7)) << 4);
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * p.scale,
+                               __uint_as_float(v[q4 * 8 + 2 * e + 1]) * p.scale);
+          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1, 128);
+    if (r == 0 && ok && *wctx.abort_flag == 0u) {
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_store_3d(&tmdQ, base + Lay::kOffQ + cb * C::kFixBlock, cb * 64, row0, bh);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+#undef FA2_BWD_WAIT
+
+// Host-side launch description.
+struct BwdLaunch {
+  CUtensorMap tmQ64, tmdO64, tmK128, tmV128, tmdK, tmdV;  // dK/dV kernel
+  CUtensorMap tmQ128, tmdO128, tmK64, tmV64, tmdQ;        // dQ kernel
+  BwdParams params;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* lse2;
+  float* dlt;
+  int causal;
+  cudaStream_t stream;
+};
+
+}  // namespace fa2

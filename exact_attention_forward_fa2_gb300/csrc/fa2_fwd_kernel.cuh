@@ -463,12 +463,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS(t);
     const uint32_t tO = tmem + lane_addr + C::kColO(t);
-    // kMod turns S into log2 units before the max, so the exponent step multiplies by 1
-    const float sl2 = kMod ? 1.0f : p.scale_log2;
-    float slope2 = 0.f;  // ALiBi slope * log2(e) of this head
+    // The exponent step computes s * sl2 - base.  With a softcap the kMod path
+    // turns S into log2 units first (sl2 = 1); otherwise S stays in raw q.k units
+    // and the ALiBi penalty is applied in those units (slope / scale).
+    const bool capped = kMod && p.cap_in > 0.f;
+    const float sl2 = capped ? 1.0f : p.scale_log2;
+    float slope_s = 0.f;  // ALiBi slope of this head, in the units S is held in
     if constexpr (kMod) {
-      if (p.alibi != nullptr)
-        slope2 = p.alibi[(bh / p.H) * p.alibi_bstride + bh % p.H] * 1.4426950408889634f;
+      if (p.alibi != nullptr) {
+        const float a = p.alibi[(bh / p.H) * p.alibi_bstride + bh % p.H];
+        slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
+      }
     }
     const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
     float m_run = -INFINITY;  // exponent base in use: a running max of scale*log2e*s
@@ -491,18 +496,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
       const int key0 = ((kMod ? span.first : kb) + j) * C::BN;
       if constexpr (kMod) {
-        // score modifiers in log2 units: softcap, then the ALiBi distance penalty
-        if (p.cap_in > 0.f) {
+        // score modifiers: softcap (into log2 units), then the ALiBi distance penalty
+        if (capped) {
 #pragma unroll
           for (int c = 0; c < C::BN; ++c) s[c] = p.cap_out * tanh_ex2(s[c] * p.cap_in);
-        } else {
-#pragma unroll
-          for (int c = 0; c < C::BN; ++c) s[c] *= p.scale_log2;
         }
-        if (slope2 != 0.f) {
+        if (slope_s != 0.f) {
           const float d0 = static_cast<float>(key0 - row);
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c) s[c] = fmaf(-slope2, fabsf(d0 + static_cast<float>(c)), s[c]);
+          for (int c = 0; c < C::BN; ++c) s[c] = fmaf(-slope_s, fabsf(d0 + static_cast<float>(c)), s[c]);
         }
         // window mask, on tiles that cross N or either window edge of some row
         const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||

@@ -55,7 +55,7 @@ extern "C" {
 #define FA2_ERR_ARCH (-8)           /* current device is not compute capability 10.3 */
 #define FA2_ERR_CUDA (-9)           /* a CUDA runtime or driver call failed */
 #define FA2_ERR_DEVICE_TIMEOUT (-10) /* a kernel gave up on a pipeline wait (see fa2_device_status) */
-#define FA2_ERR_WORKSPACE (-11)     /* split-KV workspace missing, misaligned or too small */
+#define FA2_ERR_WORKSPACE (-11)     /* workspace missing, misaligned or too small */
 #define FA2_ERR_MODIFIER (-12)      /* softcap < 0 or not finite, or alibi_batch_stride not 0 or H */
 
 /*
@@ -179,6 +179,38 @@ int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse
                 int window_right, float softcap, const float* alibi_slopes,
                 int alibi_batch_stride, int dtype, int num_splits, void* workspace,
                 size_t workspace_size, void* stream);
+
+/*
+ * fa2_bwd -- FlashAttention-2 backward pass ("From FlashAttention to
+ * FlashAttention 2", Backward Pass: Recomputation and Layer 7: The Backward
+ * Kernel; "FlashAttention-2 from PyTorch to Triton", Known gaps item 5).  Given
+ * the forward's inputs, its output o and logsumexp lse, and the upstream
+ * gradient dout = dloss/dO, writes
+ *     dq = dloss/dq,   dk = dloss/dk,   dv = dloss/dv
+ * recomputing P = exp(scale q.k - L) tile by tile:  D_i = rowsum(dout o o),
+ * dS = P (dout v^T - D),  dv = P^T dout,  dk = scale dS^T q,  dq = scale dS k.
+ * With grouped-query attention dk and dv of a key/value head sum over the query
+ * heads that read it.  dq is computed by a second pass over the keys (no
+ * atomics): results are bitwise reproducible.
+ *
+ *   q, o, dout, dq  [B,H,M,D] bf16          k, v, dk, dv  [B,H_kv,N,D] bf16
+ *   lse             [B,H,M] fp32, as written by the forward for the same inputs
+ *   causal, scale   as given to the forward
+ *   dtype           FA2_BF16 (the only type of this entry; else FA2_ERR_DTYPE)
+ *   workspace       caller-owned DEVICE buffer, 256-byte aligned, of at least
+ *                   fa2_bwd_workspace_bytes(B, H, M) bytes; scratch on return
+ * Device pointers, 16-byte aligned (lse 4-byte); dq, dk, dv are fully
+ * overwritten, everything else is only read.  Four kernels are launched on
+ * `stream`; concurrent calls must not share a workspace.  Errors as fa2_fwd_gqa,
+ * plus FA2_ERR_WORKSPACE and FA2_ERR_TOO_LARGE for M or N above 2^30.
+ */
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+            const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int M, int N,
+            int D, float scale, int causal, int dtype, void* workspace, size_t workspace_size,
+            void* stream);
+
+/* Workspace bytes fa2_bwd needs: 2 * B*H * (M rounded up to 128) * 4 (0 for invalid sizes). */
+size_t fa2_bwd_workspace_bytes(int B, int H, int M);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);
