@@ -42,8 +42,9 @@ METRIC_BWD = "FA2 bwd TFLOP/s (10BHMND, 1/2 causal) and % of GB300 dense tensor 
 BWD_FLOPS_OVER_FWD = 2.5
 UNIT = "TFLOP/s"
 KERNEL = "fa2_fwd_kernel"
-def profile_summary(workload: str) -> str:
-    return os.path.join(ROOT, "profiles", f"fa2_fwd_kernel_{workload}.md")
+def profile_summary(workload: str, pass_: str = "fwd") -> str:
+    name = f"fa2_fwd_kernel_{workload}.md" if pass_ == "fwd" else f"fa2_bwd_{workload}.md"
+    return os.path.join(ROOT, "profiles", name)
 L2_FLUSH_BYTES = 256 << 20
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tensor rates per GPU
 
@@ -57,26 +58,34 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Sources each timed pass is built from: a profile summary stays valid while these are unchanged.
+PASS_SOURCES = {
+    "fwd": ("fa2_fwd_kernel.cuh", "fa2_launch.cuh", "fa2_config.h", "sm103_ptx.cuh",
+            "fa2_fwd_bf16_d64.cu", "fa2_fwd_bf16_d128.cu", "fa2_fwd_fp32_d64.cu", "fa2_fwd_fp32_d128.cu"),
+    "bwd": ("fa2_bwd_kernel.cuh", "fa2_bwd.cu", "fa2_fwd_kernel.cuh", "sm103_ptx.cuh"),
+}
+
+
+def kernel_source_hash(pass_: str = "fwd") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_forward_fa2_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in sorted(PASS_SOURCES[pass_]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def dram_traffic_per_launch(workload: str = WORKLOAD):
-    """DRAM bytes per launch from the committed ncu summary of ``workload``, if it
-    was taken on the current kernel source (its recorded source hash matches)."""
-    path = profile_summary(workload)
+def dram_traffic_per_launch(workload: str = WORKLOAD, pass_: str = "fwd"):
+    """DRAM bytes per launch (per step, for the backward's kernels together) from
+    the committed ncu summary of ``workload``, if it was taken on the current
+    kernel source (its recorded source hash matches)."""
+    path = profile_summary(workload, pass_)
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(pass_):
         return None
     return float(m_bytes.group(1))
 
@@ -451,7 +460,7 @@ def run_ours(args, rank, local, world):
         "frac_of_peak": achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": None if bwd else dram_traffic_per_launch(w.name),
+                     "traffic": dram_traffic_per_launch(w.name, args.pass_),
                      "kernel": "fa2_bwd (preprocess + dK/dV + dQ kernels)" if bwd else KERNEL,
                      "algorithmic_flops_per_launch": flops,
                      "hbm_algorithmic_bytes_per_launch": w.io_bytes(),
