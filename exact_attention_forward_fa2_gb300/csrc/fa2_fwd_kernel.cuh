@@ -525,13 +525,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int c = 0; c < C::BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
         }
       }
-      // row max: four independent chains of 3-input max
+      // row max: four independent chains of 3-input max over s[4..BN-5], then the
+      // last four columns
       float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int c = 4; c < C::BN; c += 8) {
+      for (int c = 4; c + 8 <= C::BN; c += 8) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], s[c + q], s[c + 4 + q]);
       }
+      static_assert(C::BN % 8 == 0, "the max chains cover s[0..3], pairs of 4, then s[BN-4..BN-1]");
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mx[q] = fmaxf(mx[q], s[C::BN - 4 + q]);
       const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       const float m_new = fmaxf(m_run, m_tile);
       // Move the exponent base only when the max grew by more than 8 (factor 256):
