@@ -78,16 +78,21 @@ enum : int {
   kStatusTimeoutSoftmaxS = 7,
   kStatusTimeoutSoftmaxO = 8,
   kStatusTimeoutEpilogue = 9,
+  kStatusTimeoutSoftmaxX = 10,  // the two halves of a score row exchanging max or sum
 };
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s; a real wait lasts microseconds
 
-template <int D_, bool kBF16_, int kQTiles_, int kStages_>
+template <int D_, bool kBF16_, int kQTiles_, int kStages_, int kHalves_ = 1>
 struct FwdCfg {
   static constexpr int D = D_;
   static constexpr bool kBF16 = kBF16_;
   static constexpr int kQTiles = kQTiles_;
   static constexpr int kStages = kStages_;
+  // softmax warpgroups per query tile: 1 (a thread owns a whole score row) or 2
+  // (a thread owns 64 of its 128 keys; the two halves exchange the row max and
+  // the row sum through shared memory)
+  static constexpr int kHalves = kHalves_;
   static constexpr int BM = 128;  // query rows per tile = TMEM lanes = MMA M
   static constexpr int BN = 128;  // keys per tile = MMA N of S
   static constexpr int kElem = kBF16 ? 2 : 4;
@@ -99,7 +104,7 @@ struct FwdCfg {
   static constexpr int kStepsS = D / kMmaK;
   static constexpr int kStepsPV = BN / kMmaK;
   static constexpr int kPCols = kBF16 ? BN / 2 : BN;        // TMEM columns holding P
-  static constexpr int kSoftmaxWarps = 4 * kQTiles;
+  static constexpr int kSoftmaxWarps = 4 * kQTiles * kHalves;
   static constexpr int kMmaWarp = kSoftmaxWarps;
   static constexpr int kTmaWarp = kSoftmaxWarps + 1;
   static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
@@ -111,9 +116,12 @@ struct FwdCfg {
   static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-  static constexpr int kNumBars = 4 * kQTiles + 4 * kStages + 1;
+  static constexpr int kNumBars = 4 * kQTiles + 4 * kStages + 1 + (kHalves == 2 ? kQTiles : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // exchange buffer of the two halves: [2 parities][kQTiles][2 halves][128 rows] floats
+  static constexpr int kOffX = kOffMisc + 16;
+  static constexpr int kXBytes = kHalves == 2 ? 2 * kQTiles * 2 * 128 * 4 : 0;
+  static constexpr int kSmemBytes = kOffX + kXBytes + 1024;
   // barrier indices
   static constexpr int kBarQ = 0;
   static constexpr int kBarKFull = kBarQ + kQTiles;
@@ -124,6 +132,7 @@ struct FwdCfg {
   static constexpr int kBarPFull = kBarSFull + kQTiles;
   static constexpr int kBarOFull = kBarPFull + kQTiles;
   static constexpr int kBarMmaDone = kBarOFull + kQTiles;
+  static constexpr int kBarX = kBarMmaDone + 1;  // per tile: both halves posted (kHalves == 2)
   static constexpr uint32_t kIdescS = ptx::make_idesc(kBF16, false, BM, BN);
   static constexpr uint32_t kIdescPV = ptx::make_idesc(kBF16, true, BM, D);
 
@@ -131,6 +140,7 @@ struct FwdCfg {
   static_assert(kQTiles * (BN + D) <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kStepsS % 4 == 0 || kStepsS < 4, "K steps per 128-byte block");
+  static_assert(kHalves == 1 || kHalves == 2, "one or two softmax warpgroups per query tile");
 };
 
 // Work decode and per-tile key-tile counts (shared by all roles).
@@ -232,6 +242,276 @@ __device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Softmax role with two warpgroups per query tile (kHalves == 2): thread (r, h)
+// owns keys [64h, 64h + 64) of score row r and O columns [hD/2, hD/2 + D/2).  The
+// two halves agree on the exponent base through a bounded exchange of their
+// partial row maxima (shared memory + an mbarrier per tile), so P of one row is
+// scaled consistently for the P V product; at the end they add their partial
+// row sums the same way.
+template <class C, bool kCausal, bool kMod>
+__device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtensorMap& tmO, Unit unit,
+                                               int split, int kb, int bh, uint32_t base, uint32_t tmem,
+                                               int warp, int lane, const WaitCtx& wctx) {
+  using namespace ptx;
+  constexpr int kC = C::BN / 2;  // score columns (keys) of this thread
+  constexpr int kOC = C::D / 2;  // O columns of this thread
+  auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+  const int g = warp / 4;
+  const int t = g % C::kQTiles;
+  const int h = g / C::kQTiles;
+  const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
+  const int tile_row0 = (unit.pair * C::kQTiles + t) * C::BM;
+  const int row = tile_row0 + r;
+  const KvSpan span = kv_span<kMod>(tile_row0, p, kCausal, split);
+  const int n_t = span.count;
+  const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+  const uint32_t tS = tmem + lane_addr + C::kColS(t) + h * kC;              // S of this half
+  const uint32_t tP = tmem + lane_addr + C::kColS(t) + h * (C::kPCols / 2);  // P of this half
+  const uint32_t tO = tmem + lane_addr + C::kColO(t) + h * kOC;
+  const uint32_t xbar = bar(C::kBarX + t);
+  int xphase = 0;
+  // post `mine`, wait (bounded) until the other half has posted, read its value
+  auto exchange = [&](float mine, float& other) -> bool {
+    const uint32_t slot = base + C::kOffX + static_cast<uint32_t>((((xphase & 1) * C::kQTiles + t) * 2 + h) * 128 + r) * 4u;
+    const uint32_t peer = base + C::kOffX + static_cast<uint32_t>((((xphase & 1) * C::kQTiles + t) * 2 + (1 - h)) * 128 + r) * 4u;
+    st_shared_f32(slot, mine);
+    tc_fence_before_sync();
+    mbar_arrive(xbar);
+    const bool got = wait_bounded(xbar, static_cast<uint32_t>(xphase & 1), wctx, kStatusTimeoutSoftmaxX);
+    tc_fence_after_sync();
+    if (got) other = ld_shared_f32(peer);
+    ++xphase;
+    return got;
+  };
+  const bool capped = kMod && p.cap_in > 0.f;
+  const float sl2 = capped ? 1.0f : p.scale_log2;
+  float slope_s = 0.f;
+  if constexpr (kMod) {
+    if (p.alibi != nullptr) {
+      const float a = p.alibi[(bh / p.H) * p.alibi_bstride + bh % p.H];
+      slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
+    }
+  }
+  const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+  float m_run = -INFINITY;  // exponent base in use (the same in both halves)
+  float l_run = 0.f;        // this half's running sum of the rounded P
+  bool ok = n_t > 0;
+
+  for (int j = 0; ok && j < n_t; ++j) {
+    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + t), j & 1, wctx, kStatusTimeoutSoftmaxS));
+    if (!ok) break;
+    tc_fence_after_sync();
+    uint32_t v[2][32];
+    tmem_ld_x32(tS, v[0]);
+    tmem_ld_x32(tS + 32, v[1]);
+    tmem_ld_wait();
+    reg_fence_x32(v[0]);
+    reg_fence_x32(v[1]);
+    float s[kC];
+#pragma unroll
+    for (int c = 0; c < kC; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
+    const int key0 = ((kMod ? span.first : kb) + j) * C::BN;
+    const int keyh = key0 + h * kC;  // key of this thread's column 0
+    if constexpr (kMod) {
+      if (capped) {
+#pragma unroll
+        for (int c = 0; c < kC; ++c) s[c] = p.cap_out * tanh_ex2(s[c] * p.cap_in);
+      }
+      if (slope_s != 0.f) {
+        const float d0 = static_cast<float>(keyh - row);
+#pragma unroll
+        for (int c = 0; c < kC; ++c) s[c] = fmaf(-slope_s, fabsf(d0 + static_cast<float>(c)), s[c]);
+      }
+      const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||
+                            (key0 < tile_row0 + C::BM - 1 - p.win_left);
+      if (boundary) {
+        const int hi = min(p.N - 1, row + p.win_right) - keyh;
+        const int lo = row - p.win_left - keyh;
+#pragma unroll
+        for (int c = 0; c < kC; ++c) s[c] = (c >= lo && c <= hi) ? s[c] : -INFINITY;
+      }
+    } else {
+      const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
+      if (boundary) {
+        int lim = p.N - 1 - keyh;
+        if (kCausal) lim = min(lim, row - keyh);
+#pragma unroll
+        for (int c = 0; c < kC; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+      }
+    }
+    // max of this half (four chains), then of the whole row through the exchange
+    float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+    for (int c = 4; c + 8 <= kC; c += 8) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], s[c + q], s[c + 4 + q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mx[q] = fmaxf(mx[q], s[kC - 4 + q]);
+    const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    float mo = -INFINITY;
+    ok = __all_sync(0xffffffffu, exchange(mh, mo));
+    if (!ok) break;
+    const float m_tile = fmaxf(mh, mo) * sl2;
+    const float m_new = fmaxf(m_run, m_tile);
+    const bool rescale = (m_new - m_run) > 8.0f;
+    const float m_use = rescale ? m_new : m_run;
+    const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.0f;
+    const float neg_base = (m_use == -INFINITY) ? 0.f : -m_use;
+    const uint64_t nb2 = pack_f32x2(neg_base, neg_base);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < kC / 2; ++i) {
+      const int c = 2 * i;
+      float x0, x1;
+      unpack_f32x2(ffma2(pack_f32x2(s[c], s[c + 1]), sl2x2, nb2), x0, x1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if constexpr (C::kBF16) {
+        const uint32_t w = pack_bf16x2(p0, p1);
+        pk[i] = w;
+        acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+      } else {
+        const uint32_t r0 = round_tf32(p0), r1 = round_tf32(p1);
+        s[c] = __uint_as_float(r0);
+        s[c + 1] = __uint_as_float(r1);
+        acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(s[c], s[c + 1]));
+      }
+    }
+    if constexpr (C::kBF16) {
+      tmem_st_x32(tP, pk);  // 64 keys -> 32 columns of bf16x2
+    } else {
+      uint32_t q0[32], q1[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        q0[i] = __float_as_uint(s[i]);
+        q1[i] = __float_as_uint(s[32 + i]);
+      }
+      tmem_st_x32(tP, q0);
+      tmem_st_x32(tP + 32, q1);
+    }
+    float a0, a1, a2, a3, a4, a5, a6, a7;
+    unpack_f32x2(acc[0], a0, a1);
+    unpack_f32x2(acc[1], a2, a3);
+    unpack_f32x2(acc[2], a4, a5);
+    unpack_f32x2(acc[3], a6, a7);
+    l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+    if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (j - 1) & 1, wctx, kStatusTimeoutSoftmaxO));
+      if (!ok) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int ch = 0; ch < kOC / 32; ++ch) {
+        uint32_t o[32];
+        tmem_ld_x32(tO + ch * 32, o);
+        tmem_ld_wait();
+        reg_fence_x32(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st_x32(tO + ch * 32, o);
+      }
+    }
+    tmem_st_wait();
+    tc_fence_before_sync();
+    mbar_arrive(bar(C::kBarPFull + t));
+    m_run = m_use;
+  }
+
+  // ------------------------------------------------------------ epilogue
+  if (p.num_splits > 1) {
+    if (tile_row0 < p.M) {
+      if (n_t > 0 && ok)
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx, kStatusTimeoutEpilogue));
+      float lo_sum = 0.f;
+      if (n_t > 0 && ok) ok = __all_sync(0xffffffffu, exchange(l_run, lo_sum));
+      const float l_tot = l_run + lo_sum;
+      const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh) * p.M + row;
+      float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D + h * kOC);
+      if (n_t > 0 && ok) {
+        tc_fence_after_sync();
+        const float inv_l = l_tot > 0.f ? 1.0f / l_tot : 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kOC / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_x32(tO + ch * 32, v);
+          tmem_ld_wait();
+          reg_fence_x32(v);
+          if (row < p.M) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              op[ch * 8 + q4] = make_float4(__uint_as_float(v[q4 * 4 + 0]) * inv_l, __uint_as_float(v[q4 * 4 + 1]) * inv_l,
+                                            __uint_as_float(v[q4 * 4 + 2]) * inv_l, __uint_as_float(v[q4 * 4 + 3]) * inv_l);
+          }
+        }
+        if (row < p.M && h == 0) p.l_part[prow] = (m_run + lg2_approx(l_tot)) * 0.69314718055994530942f;
+      } else if (n_t == 0 && row < p.M) {
+#pragma unroll
+        for (int q4 = 0; q4 < kOC / 4; ++q4) op[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (h == 0) p.l_part[prow] = -INFINITY;
+      }
+    }
+  } else if (n_t > 0 || (kMod && tile_row0 < p.M)) {
+    if (ok)
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx, kStatusTimeoutEpilogue));
+    float lo_sum = 0.f;
+    if (ok) ok = __all_sync(0xffffffffu, exchange(l_run, lo_sum));
+    const float l_tot = l_run + lo_sum;
+    const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
+    constexpr int kChunks = C::kColBlocks * 8;  // 16-byte chunks of one O row
+    if (kMod && n_t == 0) {
+#pragma unroll
+      for (int cidx = h * kChunks / 2; cidx < (h + 1) * kChunks / 2; ++cidx)
+        st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
+      if (row < p.M && h == 0) p.lse[static_cast<int64_t>(bh) * p.M + row] = -INFINITY;
+    } else if (ok) {
+      tc_fence_after_sync();
+      const float inv_l = l_tot > 0.f ? 1.0f / l_tot : 0.f;
+#pragma unroll
+      for (int chl = 0; chl < kOC / 32; ++chl) {
+        const int ch = h * (kOC / 32) + chl;  // 32-column group of the whole O row
+        uint32_t v[32];
+        tmem_ld_x32(tO + chl * 32, v);
+        tmem_ld_wait();
+        reg_fence_x32(v);
+        if constexpr (C::kBF16) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int cidx = ch * 4 + q4;
+            const int cb = cidx / 8, c = cidx % 8;
+            const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * inv_l, __uint_as_float(v[q4 * 8 + 2 * e + 1]) * inv_l);
+            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {
+            const int cb = ch, c = q8;
+            const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+            st_shared_v4(addr, __float_as_uint(__uint_as_float(v[q8 * 4 + 0]) * inv_l),
+                         __float_as_uint(__uint_as_float(v[q8 * 4 + 1]) * inv_l),
+                         __float_as_uint(__uint_as_float(v[q8 * 4 + 2]) * inv_l),
+                         __float_as_uint(__uint_as_float(v[q8 * 4 + 3]) * inv_l));
+          }
+        }
+      }
+      if (row < p.M && h == 0)
+        p.lse[static_cast<int64_t>(bh) * p.M + row] = (m_run + lg2_approx(l_tot)) * 0.69314718055994530942f;
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1 + t, 256);
+    if (r == 0 && h == 0 && *wctx.abort_flag == 0u) {
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+  }
+}
+
 template <class C, bool kCausal, bool kMod>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -292,7 +572,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (int t = 0; t < C::kQTiles; ++t) {
       mbar_init(bar(C::kBarQ + t), 1);
       mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), 128);
+      mbar_init(bar(C::kBarPFull + t), 128 * C::kHalves);
+      if (C::kHalves == 2) mbar_init(bar(C::kBarX + t), 256);
       mbar_init(bar(C::kBarOFull + t), 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -452,6 +733,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       drain_bounded(bar(C::kBarMmaDone), 0);
     }
     __syncwarp();
+  } else if (!skip && warp < C::kSoftmaxWarps && C::kHalves == 2) {
+    softmax_halves<C, kCausal, kMod>(p, tmO, unit, split, kb, bh, base, tmem, warp, lane, wctx);
   } else if (!skip && warp < C::kSoftmaxWarps) {
     // ---------------------------------------------------------- softmax warpgroups
     const int t = warp / 4;
