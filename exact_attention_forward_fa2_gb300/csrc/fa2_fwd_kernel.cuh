@@ -100,6 +100,15 @@ struct FwdCfg {
   static constexpr int kColBlocks = D / kSwElems;           // 128-byte column blocks per row
   static constexpr int kBlockBytes = 128 * 128;             // 128 rows x 128 bytes
   static constexpr int kTileBytes = kColBlocks * kBlockBytes;
+  // D = 64 (one softmax warpgroup per tile): the P V product also forms the row
+  // sum l.  Every V stage carries one more 128-byte column block filled with ones,
+  // the P V GEMM runs with N = D + 16, and O_t holds [O | 16 copies of l]: the sum
+  // of the rounded P the tensor core used, accumulated in fp32 and rescaled with O,
+  // at no cost on the CUDA cores.  (At D = 128 the 16 extra TMEM columns per tile
+  // do not fit beside S and O of two tiles.)
+  static constexpr bool kLOnes = (D == 64 && kHalves == 1);
+  static constexpr int kOW = kLOnes ? D + 16 : D;  // TMEM columns of O_t
+  static constexpr int kVTileBytes = (kColBlocks + (kLOnes ? 1 : 0)) * kBlockBytes;
   static constexpr int kMmaK = 32 / kElem;                  // one MMA consumes 32 bytes of K
   static constexpr int kStepsS = D / kMmaK;
   static constexpr int kStepsPV = BN / kMmaK;
@@ -110,12 +119,12 @@ struct FwdCfg {
   static constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
   static constexpr uint32_t kTmemCols = 512;
   __host__ __device__ static constexpr int kColS(int t) { return t * BN; }
-  __host__ __device__ static constexpr int kColO(int t) { return kQTiles * BN + t * D; }
+  __host__ __device__ static constexpr int kColO(int t) { return kQTiles * BN + t * kOW; }
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kVTileBytes;
   static constexpr int kNumBars = 4 * kQTiles + 4 * kStages + 1 + (kHalves == 2 ? kQTiles : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // exchange buffer of the two halves: [2 parities][kQTiles][2 halves][128 rows] floats
@@ -134,10 +143,10 @@ struct FwdCfg {
   static constexpr int kBarMmaDone = kBarOFull + kQTiles;
   static constexpr int kBarX = kBarMmaDone + 1;  // per tile: both halves posted (kHalves == 2)
   static constexpr uint32_t kIdescS = ptx::make_idesc(kBF16, false, BM, BN);
-  static constexpr uint32_t kIdescPV = ptx::make_idesc(kBF16, true, BM, D);
+  static constexpr uint32_t kIdescPV = ptx::make_idesc(kBF16, true, BM, kOW);
 
   static_assert(D % kSwElems == 0, "head dim must fill whole 128-byte rows");
-  static_assert(kQTiles * (BN + D) <= 512, "TMEM budget");
+  static_assert(kQTiles * (BN + kOW) <= 512, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kStepsS % 4 == 0 || kStepsS < 4, "K steps per 128-byte block");
   static_assert(kHalves == 1 || kHalves == 2, "one or two softmax warpgroups per query tile");
@@ -595,6 +604,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     tmem_alloc(base + C::kOffMisc, C::kTmemCols);
     tmem_relinquish_alloc_permit();
   }
+  if constexpr (C::kLOnes) {
+    // the ones block of every V stage (TMA writes only the blocks before it)
+    const uint32_t one2 = C::kBF16 ? 0x3F803F80u : 0x3F800000u;
+    for (int i = static_cast<int>(threadIdx.x); i < C::kStages * (C::kBlockBytes / 16); i += C::kThreads) {
+      const int st = i / (C::kBlockBytes / 16), o = i % (C::kBlockBytes / 16);
+      st_shared_v4(base + C::kOffV + st * C::kVTileBytes + C::kColBlocks * C::kBlockBytes + o * 16, one2, one2,
+                   one2, one2);
+    }
+    fence_proxy_async_smem();  // visible to the tensor core (async proxy)
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -634,7 +653,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d_hint(base + C::kOffV + s * C::kTileBytes + cb * C::kBlockBytes, &tmV,
+          tma_load_3d_hint(base + C::kOffV + s * C::kVTileBytes + cb * C::kBlockBytes, &tmV,
                            bar(C::kBarVFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
         issued = j + 1;
       }
@@ -675,7 +694,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               v_ready = true;
             }
             tc_fence_after_sync();
-            const uint32_t v_base = base + C::kOffV + sv * C::kTileBytes;
+            const uint32_t v_base = base + C::kOffV + sv * C::kVTileBytes;
             const int jp0 = kMod ? jb[t] : 0;  // first P V of this tile overwrites O
 #pragma unroll
             for (int kk = 0; kk < C::kStepsPV; ++kk) {
@@ -845,13 +864,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           if constexpr (C::kBF16) {
             const uint32_t w = pack_bf16x2(p0, p1);
             pk[i] = w;
-            acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(__uint_as_float(w << 16),
-                                                      __uint_as_float(w & 0xffff0000u)));
+            if constexpr (!C::kLOnes)
+              acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(__uint_as_float(w << 16),
+                                                        __uint_as_float(w & 0xffff0000u)));
           } else {
             const uint32_t r0 = round_tf32(p0), r1 = round_tf32(p1);
             s[c] = __uint_as_float(r0);
             s[c + 1] = __uint_as_float(r1);
-            acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(s[c], s[c + 1]));
+            if constexpr (!C::kLOnes) acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(s[c], s[c + 1]));
           }
         }
         if constexpr (C::kBF16) {
@@ -867,12 +887,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tmem_st_x32(tS + h * 64 + 32, q1);
         }
       }
-      float a0, a1, a2, a3, a4, a5, a6, a7;
-      unpack_f32x2(acc[0], a0, a1);
-      unpack_f32x2(acc[1], a2, a3);
-      unpack_f32x2(acc[2], a4, a5);
-      unpack_f32x2(acc[3], a6, a7);
-      l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+      if constexpr (!C::kLOnes) {
+        float a0, a1, a2, a3, a4, a5, a6, a7;
+        unpack_f32x2(acc[0], a0, a1);
+        unpack_f32x2(acc[1], a2, a3);
+        unpack_f32x2(acc[2], a4, a5);
+        unpack_f32x2(acc[3], a6, a7);
+        l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+      }
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O_t *= alpha once P_{j-1} V_{j-1} has landed in TMEM
         ok = __all_sync(0xffffffffu,
@@ -889,12 +911,34 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st_x32(tO + ch * 32, o);
         }
+        if constexpr (C::kLOnes) {  // the row sum columns scale with O
+          uint32_t o[16];
+          tmem_ld_x16(tO + C::D, o);
+          tmem_ld_wait();
+          reg_fence_x16(o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_x16(tO + C::D, o);
+        }
       }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(C::kBarPFull + t));
       m_run = m_use;
     }
+    // With the ones column the row sum is read from O_t's column D once the last
+    // P V has landed (the epilogue waits for it before using l_run).
+    auto row_sum = [&]() -> float {
+      if constexpr (C::kLOnes) {
+        uint32_t lv[16];
+        tmem_ld_x16(tO + C::D, lv);
+        tmem_ld_wait();
+        reg_fence_x16(lv);
+        return __uint_as_float(lv[0]);
+      } else {
+        return l_run;
+      }
+    };
 
     // ------------------------------------------------------------ epilogue
     if (p.num_splits > 1) {
@@ -908,6 +952,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D);
         if (n_t > 0 && ok) {
           tc_fence_after_sync();
+          l_run = row_sum();
           const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll
           for (int ch = 0; ch < C::D / 32; ++ch) {
@@ -947,6 +992,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (row < p.M) p.lse[static_cast<int64_t>(bh) * p.M + row] = -INFINITY;
       } else if (ok) {
         tc_fence_after_sync();
+        l_run = row_sum();
         const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
 #pragma unroll
         for (int ch = 0; ch < C::D / 32; ++ch) {
