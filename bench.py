@@ -302,11 +302,12 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def measure_e2e(args, flops, step, stream, world, ins, outs):
+def measure_e2e(args, flops, step, stream, world, ins, outs, host_step=None):
     """Same metric end to end: each step copies the step's inputs from pinned host
     memory (``ins``: pairs of host array and its device tensor), runs the pass
     through the C ABI and copies the results (``outs``) back to pinned host
-    memory, all inside the timed region."""
+    memory, all inside the timed region.  ``host_step(host_ins, host_outs)``, when
+    given, is one call of the library's host-buffer entry doing all three."""
     import torch
 
     def raw(t):
@@ -319,6 +320,9 @@ def measure_e2e(args, flops, step, stream, world, ins, outs):
     houts = [(torch.empty(t.shape, dtype=raw(t).dtype).pin_memory(), raw(t)) for t in outs]
 
     def e2e_step():
+        if host_step is not None:
+            host_step([h for h, _ in pairs], [h for h, _ in houts])
+            return
         for h, d in pairs:
             d.copy_(h, non_blocking=True)
         step()
@@ -433,7 +437,16 @@ def run_ours(args, rank, local, world):
         o_host = o.view(torch.int16).cpu().numpy().view(np.uint16)
         e2e_ins = [(q, tq), (k, tk), (v, tv), (o_host, o), (lse.cpu().numpy(), lse), (do, tdo)]
         e2e_outs = [dq, dk, dv]
-    e2e = measure_e2e(args, flops, step, stream, world, e2e_ins, e2e_outs) if args.e2e else None
+    host_step = None
+    if not (bwd or w.modified or w.split_kv):
+        def host_step(hin, hout):
+            as_dt = (lambda t: t.view(torch.bfloat16)) if w.dtype == si.BF16 else (lambda t: t)
+            fa2.fa2_fwd_host(as_dt(hin[0]), as_dt(hin[1]), as_dt(hin[2]), o_host=as_dt(hout[0]),
+                             lse_host=hout[1], q=tq, k=tk, v=tv, o=o, lse=lse, scale=w.scale,
+                             causal=w.causal, chunks=args.e2e_chunks, stream=stream)
+    e2e = measure_e2e(args, flops, step, stream, world, e2e_ins, e2e_outs, host_step) if args.e2e else None
+    if e2e is not None:
+        e2e["api"] = "fa2_fwd_host (pipelined copies)" if host_step else "copies + device-buffer call"
 
     if rank != 0:
         return
@@ -498,6 +511,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="head slices of the host-buffer pipeline (0: the library's choice)")
     ap.add_argument("--clock-log", default=None, help="write the NVML clock samples here (CSV)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

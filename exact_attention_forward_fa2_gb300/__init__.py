@@ -47,6 +47,8 @@ SIGNATURES = {
     "fa2_bwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ,
                  _VP], _I),
     "fa2_bwd_workspace_bytes": ([_I, _I, _I], _SZ),
+    "fa2_fwd_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                      _I, _VP], _I),
     "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I], _I),
     "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "fa2_strerror": ([_I], ctypes.c_char_p),
@@ -226,6 +228,59 @@ def fa2_fwd_ext(q, k, v, o=None, lse=None, scale: float | None = None, causal: b
     if rc != FA2_OK:
         raise Fa2Error(rc, "fa2_fwd_ext")
     return o, lse
+
+
+def fa2_fwd_host(q_host, k_host, v_host, o_host=None, lse_host=None, q=None, k=None, v=None, o=None,
+                 lse=None, scale: float | None = None, causal: bool = False, chunks: int = 0,
+                 device=None, stream=None):
+    """Forward for host tensors (C ABI ``fa2_fwd_host``): copies in, computes and
+    copies out in slices of heads that overlap one another.  ``q_host`` etc. are
+    CPU tensors (page-locked for overlap); the device buffers ``q, k, v, o, lse``
+    are allocated on ``device`` (default: the current CUDA device) when not given.
+    Returns (o_host, lse_host); they are valid once ``stream`` is synchronised."""
+    import torch
+
+    if q_host.is_cuda or k_host.is_cuda or v_host.is_cuda:
+        raise ValueError("q_host, k_host, v_host must be host tensors")
+    if q_host.dim() != 4 or k_host.dim() != 4 or v_host.shape != k_host.shape \
+            or q_host.shape[0] != k_host.shape[0] or q_host.shape[3] != k_host.shape[3] \
+            or q_host.shape[1] % k_host.shape[1] != 0:
+        raise ValueError("expected q [B,H,M,D] and k, v [B,H_kv,N,D] with H_kv dividing H")
+    if q_host.dtype not in (torch.bfloat16, torch.float32) or k_host.dtype != q_host.dtype \
+            or v_host.dtype != q_host.dtype:
+        raise TypeError("q, k, v must share one dtype, bf16 or fp32")
+    for t in (q_host, k_host, v_host):
+        if not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous")
+    dtype = FA2_BF16 if q_host.dtype == torch.bfloat16 else FA2_FP32
+    B, H, M, D = q_host.shape
+    H_kv, N = k_host.shape[1], k_host.shape[2]
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if o_host is None:
+        o_host = torch.empty(q_host.shape, dtype=q_host.dtype).pin_memory()
+    if lse_host is None:
+        lse_host = torch.empty((B, H, M), dtype=torch.float32).pin_memory()
+    q = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev) if q is None else q
+    k = torch.empty(k_host.shape, dtype=k_host.dtype, device=dev) if k is None else k
+    v = torch.empty(v_host.shape, dtype=v_host.dtype, device=dev) if v is None else v
+    o = torch.empty(q_host.shape, dtype=q_host.dtype, device=dev) if o is None else o
+    lse = torch.empty((B, H, M), dtype=torch.float32, device=dev) if lse is None else lse
+    for t, like in ((q, q_host), (k, k_host), (v, v_host), (o, q_host), (o_host, q_host)):
+        if t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
+            raise ValueError("buffers must match the shapes and dtype of q_host / k_host")
+    if lse.shape != (B, H, M) or lse_host.shape != (B, H, M) or lse.dtype != torch.float32 \
+            or lse_host.dtype != torch.float32:
+        raise ValueError("lse buffers must be fp32 [B,H,M]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        rc = lib().fa2_fwd_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+                                lse_host.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), B, H, H_kv, M, N, D, float(scale), 1 if causal else 0, dtype,
+                                int(chunks), _stream_handle(q, stream))
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_fwd_host")
+    return o_host, lse_host
 
 
 def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool = False,

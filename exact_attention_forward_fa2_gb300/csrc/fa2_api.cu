@@ -233,6 +233,36 @@ size_t bwd_workspace_bytes(int64_t bh, int M) {
   return 2 * static_cast<size_t>(bh * mpad) * sizeof(float);
 }
 
+// Streams and events of the host-buffer pipeline (fa2_fwd_host), created once
+// per device; the whole enqueue sequence of one call holds the mutex.
+constexpr int kHostMaxChunks = 32;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, out_done = nullptr;
+  cudaEvent_t in[kHostMaxChunks] = {};
+  cudaEvent_t done[kHostMaxChunks] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    bool ok = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.out_done, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; ok && c < kHostMaxChunks; ++c)
+      ok = cudaEventCreateWithFlags(&hp.in[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return FA2_ERR_CUDA;
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA2_OK;
+}
+
 int sm_count(int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
@@ -299,6 +329,79 @@ extern "C" int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o,
   mods.alibi_bstride = alibi_batch_stride;
   return run_forward(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, causal, dtype, num_splits,
                      workspace, workspace_size, stream, mods);
+}
+
+extern "C" int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                            float* lse_host, void* q, void* k, void* v, void* o, float* lse, int B,
+                            int H, int H_kv, int M, int N, int D, float scale, int causal, int dtype,
+                            int chunks, void* stream) {
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host) return FA2_ERR_NULL;
+  // every argument of the device-side call is checked once for the whole problem
+  // (a call with num_splits = 1 that stops before any CUDA work on error)
+  if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
+  if (D != 64 && D != 128) return FA2_ERR_HEADDIM;
+  if (dtype != FA2_BF16 && dtype != FA2_FP32) return FA2_ERR_DTYPE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
+  const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+  if ((addr(q) | addr(k) | addr(v) | addr(o)) & 15u) return FA2_ERR_ALIGN;
+  if (addr(lse) & 3u) return FA2_ERR_ALIGN;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh > INT_MAX) return FA2_ERR_TOO_LARGE;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != FA2_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+
+  // chunk unit: one key/value head with the query heads that read it (flat
+  // index b*H_kv + j; its query heads are the contiguous flat heads
+  // [group*(b*H_kv + j), +group) of q, o and lse)
+  const int group = H / H_kv;
+  const int64_t kv_heads = static_cast<int64_t>(B) * H_kv;
+  if (chunks <= 0) chunks = 4;
+  chunks = static_cast<int>(std::min<int64_t>({static_cast<int64_t>(chunks), kv_heads, kHostMaxChunks}));
+  const size_t e = dtype == FA2_BF16 ? 2 : 4;
+  const size_t q_head = static_cast<size_t>(M) * D * e, kv_head = static_cast<size_t>(N) * D * e;
+  const size_t l_head = static_cast<size_t>(M) * sizeof(float);
+  const cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  auto at = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+  auto atw = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(dev, &hp);
+  if (rc != FA2_OK) return rc;
+  bool ok = cudaEventRecord(hp->start, s0) == cudaSuccess &&  // after the caller's earlier work
+            cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess;
+  for (int c = 0; ok && c < chunks; ++c) {
+    const int64_t g0 = kv_heads * c / chunks, g1 = kv_heads * (c + 1) / chunks;
+    const int64_t nq = (g1 - g0) * group, q0 = g0 * group;
+    ok = cudaMemcpyAsync(atw(q, q0 * q_head), at(q_host, q0 * q_head), nq * q_head, cudaMemcpyHostToDevice,
+                         hp->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(atw(k, g0 * kv_head), at(k_host, g0 * kv_head), (g1 - g0) * kv_head,
+                         cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(atw(v, g0 * kv_head), at(v_host, g0 * kv_head), (g1 - g0) * kv_head,
+                         cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
+         cudaEventRecord(hp->in[c], hp->h2d) == cudaSuccess &&
+         cudaStreamWaitEvent(s0, hp->in[c], 0) == cudaSuccess;
+    if (!ok) break;
+    // these heads as a problem of their own: batch 1, nq query heads, g1 - g0 key/value heads
+    rc = run_forward(at(q, q0 * q_head), at(k, g0 * kv_head), at(v, g0 * kv_head), atw(o, q0 * q_head),
+                     lse + q0 * M, 1, static_cast<int>(nq), static_cast<int>(g1 - g0), M, N, D, scale, causal,
+                     dtype, 1, nullptr, 0, s0);
+    if (rc != FA2_OK) return rc;
+    ok = cudaEventRecord(hp->done[c], s0) == cudaSuccess &&
+         cudaStreamWaitEvent(hp->d2h, hp->done[c], 0) == cudaSuccess &&
+         cudaMemcpyAsync(atw(o_host, q0 * q_head), at(o, q0 * q_head), nq * q_head, cudaMemcpyDeviceToHost,
+                         hp->d2h) == cudaSuccess &&
+         cudaMemcpyAsync(lse_host + q0 * M, lse + q0 * M, nq * l_head, cudaMemcpyDeviceToHost, hp->d2h) ==
+             cudaSuccess;
+  }
+  // the caller's stream reaches its next work only after the last copy back
+  ok = ok && cudaEventRecord(hp->out_done, hp->d2h) == cudaSuccess &&
+       cudaStreamWaitEvent(s0, hp->out_done, 0) == cudaSuccess;
+  return ok ? FA2_OK : FA2_ERR_CUDA;
 }
 
 extern "C" int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,

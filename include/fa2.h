@@ -212,6 +212,33 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const fl
 /* Workspace bytes fa2_bwd needs: 2 * B*H * (M rounded up to 128) * 4 (0 for invalid sizes). */
 size_t fa2_bwd_workspace_bytes(int B, int H, int M);
 
+/*
+ * fa2_fwd_host -- the forward for inputs and outputs in HOST memory.  Copies q,
+ * k, v from host to the caller's device buffers, runs the forward and copies o
+ * and lse back, cut into `chunks` slices of heads (each slice: whole key/value
+ * heads with the query heads that read them) so that the copy of one slice
+ * overlaps the compute of the previous one and the copy back of the one before.
+ * Copies to the device run on a library stream, the kernels on `stream`, copies
+ * back on a second library stream; `stream` reaches its next work only after the
+ * last copy back, so synchronising `stream` makes o_host and lse_host valid.
+ *
+ *   q_host, k_host, v_host  [B,H,M,D] / [B,H_kv,N,D] inputs in host memory, only read
+ *   o_host, lse_host        [B,H,M,D] / [B,H,M] fp32 outputs in host memory, overwritten
+ *   q, k, v, o, lse         DEVICE buffers of the same shapes (caller-owned, as
+ *                           fa2_fwd_gqa); q, k, v are overwritten by the copies
+ *   chunks                  slices (<= 0: 4); at most B*H_kv and 32
+ * Host buffers should be page-locked (cudaHostAlloc or cudaHostRegister): the
+ * copies from pageable memory do not overlap anything.  Other arguments and
+ * errors as fa2_fwd_gqa.  The library's two copy streams and their events are
+ * created on the first call on a device (not during stream capture); calls on
+ * one device are enqueued one at a time.  The pages have no counterpart to this
+ * entry: it is the host-side pipelining of the same forward.
+ */
+int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                 float* lse_host, void* q, void* k, void* v, void* o, float* lse, int B, int H,
+                 int H_kv, int M, int N, int D, float scale, int causal, int dtype, int chunks,
+                 void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);
 

@@ -32,7 +32,7 @@ def lib():
 
 def test_header_declares_the_api():
     assert declared_functions() == ["fa2_bwd", "fa2_bwd_workspace_bytes", "fa2_device_status", "fa2_fwd",
-                                    "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_splitkv",
+                                    "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_host", "fa2_fwd_splitkv",
                                     "fa2_fwd_splitkv_noalloc", "fa2_splitkv_num_splits",
                                     "fa2_splitkv_workspace_bytes", "fa2_strerror", "fa2_version"]
 
@@ -179,6 +179,24 @@ def test_bwd_workspace_bytes(lib):
 ])
 def test_bwd_rejects_bad_arguments(lib, kw, code):
     assert call_bwd(lib, **kw) == code
+
+
+def call_host(lib, **kw):
+    a = dict(qh=P, kh=P, vh=P, oh=P, lh=P, q=P, k=P, v=P, o=P, lse=P, B=2, H=4, H_kv=2, M=64, N=64, D=64,
+             scale=0.125, causal=0, dtype=0, chunks=0)
+    a.update(kw)
+    return lib.fa2_fwd_host(a["qh"], a["kh"], a["vh"], a["oh"], a["lh"], a["q"], a["k"], a["v"], a["o"],
+                            a["lse"], a["B"], a["H"], a["H_kv"], a["M"], a["N"], a["D"], a["scale"],
+                            a["causal"], a["dtype"], a["chunks"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(qh=None), fa2.FA2_ERR_NULL), (dict(lh=None), fa2.FA2_ERR_NULL), (dict(o=None), fa2.FA2_ERR_NULL),
+    (dict(H_kv=3), fa2.FA2_ERR_SHAPE), (dict(D=32), fa2.FA2_ERR_HEADDIM), (dict(dtype=5), fa2.FA2_ERR_DTYPE),
+    (dict(scale=-1.0), fa2.FA2_ERR_SCALE), (dict(v=P + 4), fa2.FA2_ERR_ALIGN),
+])
+def test_host_entry_rejects_bad_arguments(lib, kw, code):
+    assert call_host(lib, **kw) == code
 
 
 def test_no_gpu_means_an_error_not_a_fallback(lib):
