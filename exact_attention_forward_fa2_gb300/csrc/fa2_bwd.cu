@@ -23,16 +23,16 @@ cudaError_t launch_dkdv(BwdLaunch& L, bool& attr_done) {
 
 template <class C, bool kCausal>
 cudaError_t launch_dq(BwdLaunch& L, bool& attr_done) {
-  using Lay = DqLayout<C>;
   if (!attr_done) {
     const cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<C, kCausal>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  const dim3 grid(static_cast<unsigned>(L.params.BH * L.params.n_qtiles));
-  bwd_dq_kernel<C, kCausal><<<grid, C::kThreads, Lay::kSmemBytes, L.stream>>>(L.tmQ128, L.tmdO128, L.tmK64,
-                                                                             L.tmV64, L.tmdQ, L.params);
+  const int pairs = (L.params.n_qtiles + C::kQT - 1) / C::kQT;
+  const dim3 grid(static_cast<unsigned>(L.params.BH * pairs));
+  bwd_dq_kernel<C, kCausal><<<grid, C::kThreads, C::kSmemBytes, L.stream>>>(L.tmQ128, L.tmdO128, L.tmK64,
+                                                                           L.tmV64, L.tmdQ, L.params);
   return cudaGetLastError();
 }
 
@@ -51,7 +51,8 @@ cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
   bool* a = attr[dev];
   e = L.causal ? launch_dkdv<C, true>(L, a[1]) : launch_dkdv<C, false>(L, a[0]);
   if (e != cudaSuccess) return e;
-  return L.causal ? launch_dq<C, true>(L, a[3]) : launch_dq<C, false>(L, a[2]);
+  using CQ = DqCfg<D, D == 64 ? 4 : 3>;  // two query tiles per CTA; K/V ring as deep as fits
+  return L.causal ? launch_dq<CQ, true>(L, a[3]) : launch_dq<CQ, false>(L, a[2]);
 }
 
 }  // namespace

@@ -443,28 +443,67 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ dQ
-template <class C>
-struct DqLayout {
-  // shared memory: Q, dO (fixed, 128 rows), then kStages x {K, V (64 rows)}
+// Two 128-row query tiles per CTA share every streamed 64-row K/V step and
+// ping-pong on the tensor core like the forward: while warpgroup t forms dS of
+// tile t, the MMA thread runs the other tile's GEMMs.  TMEM per tile t (256
+// columns): S_t [256 t, +64) (dS_t overwrites its first 32 as packed bf16),
+// dP_t [256 t + 64, +64), dQ_t [256 t + 128, +D).
+template <int D_, int kStages_>
+struct DqCfg {
+  static constexpr int D = D_;
+  static constexpr int kStages = kStages_;
+  static constexpr int kQT = 2;              // query tiles per CTA
+  static constexpr int BF = 128;             // rows of a query tile
+  static constexpr int BS = 64;              // keys per step
+  static constexpr int kColBlocks = D / 64;
+  static constexpr int kFixBlock = BF * 128;
+  static constexpr int kStrBlock = BS * 128;
+  static constexpr int kFixTile = kColBlocks * kFixBlock;
+  static constexpr int kStrTile = kColBlocks * kStrBlock;
+  static constexpr int kMmaK = 16;
+  static constexpr int kStepsD = D / kMmaK;
+  static constexpr int kSoftWarps = 4 * kQT;
+  static constexpr int kThreads = (kSoftWarps + 2) * 32;
+  static constexpr int kMmaWarp = kSoftWarps;
+  static constexpr int kTmaWarp = kSoftWarps + 1;
+  static constexpr uint32_t kTmemCols = 512;
+  __host__ __device__ static constexpr int kColS(int t) { return 256 * t; }
+  __host__ __device__ static constexpr int kColDP(int t) { return 256 * t + 64; }
+  __host__ __device__ static constexpr int kColQ(int t) { return 256 * t + 128; }
+  static constexpr uint32_t kIdescS = ptx::make_idesc(true, false, BF, BS);
+  static constexpr uint32_t kIdescAcc = ptx::make_idesc(true, true, BF, D);
+  // shared memory: Q[2], dO[2] (fixed), then kStages x {K, V} (64 rows)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffDO = kOffQ + C::kFixTile;
-  static constexpr int kOffRing = kOffDO + C::kFixTile;
-  static constexpr int kStageBytes = 2 * C::kStrTile;
-  static_assert(kStageBytes % 1024 == 0, "stage alignment");
-  static constexpr int kOffBar = kOffRing + C::kStages * kStageBytes;
+  static constexpr int kOffDO = kOffQ + kQT * kFixTile;
+  static constexpr int kOffRing = kOffDO + kQT * kFixTile;
+  static constexpr int kStageBytes = 2 * kStrTile;
+  static constexpr int kOffBar = kOffRing + kStages * kStageBytes;
+  // barriers: Q[2], full[S], empty[S], sfull[2], pfull[2], done
   static constexpr int kBarQ = 0;
-  static constexpr int kBarFull = 1;
-  static constexpr int kBarEmpty = kBarFull + C::kStages;
-  static constexpr int kBarSFull = kBarEmpty + C::kStages;
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarDone = kBarPFull + 2;
+  static constexpr int kBarFull = kBarQ + kQT;
+  static constexpr int kBarEmpty = kBarFull + kStages;
+  static constexpr int kBarSFull = kBarEmpty + kStages;
+  static constexpr int kBarPFull = kBarSFull + kQT;
+  static constexpr int kBarDone = kBarPFull + kQT;
   static constexpr int kNumBars = kBarDone + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
   __host__ __device__ static constexpr int k_off(int s) { return kOffRing + s * kStageBytes; }
-  __host__ __device__ static constexpr int v_off(int s) { return k_off(s) + C::kStrTile; }
+  __host__ __device__ static constexpr int v_off(int s) { return k_off(s) + kStrTile; }
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kColQ(kQT - 1) + D <= 512, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kStageBytes % 1024 == 0 && kFixTile % 1024 == 0, "1024-byte aligned tiles");
 };
+
+// Keys [0, end) that some row of the query tile starting at row0 sees; 0 if the
+// tile is past M.
+template <bool kCausal>
+__device__ __forceinline__ int dq_key_end(int row0, int M, int N) {
+  if (row0 >= M) return 0;
+  const int last_row = min(row0 + 128, M) - 1;
+  return kCausal ? min(N, last_row + 1) : N;
+}
 
 template <class C, bool kCausal>
 __global__ void __launch_bounds__(C::kThreads, 1)
@@ -472,45 +511,49 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmdQ, const BwdParams p) {
   using namespace ptx;
-  using Lay = DqLayout<C>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + Lay::kOffMisc);
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::kOffMisc);
   const int warp = static_cast<int>(threadIdx.x) / 32;
   const int lane = static_cast<int>(threadIdx.x) % 32;
-  auto bar = [&](int i) -> uint32_t { return base + Lay::kOffBar + 8u * static_cast<uint32_t>(i); };
+  auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
 
-  // unit: causal tiles longest first (largest query tile), else one head's tiles adjacent
+  // unit: (head, pair of query tiles); causal pairs longest first, else one head's pairs adjacent
+  const int pairs = (p.n_qtiles + C::kQT - 1) / C::kQT;
   const int b = static_cast<int>(blockIdx.x);
-  int bh, qt;
+  int bh, pair;
   if (kCausal) {
-    qt = p.n_qtiles - 1 - b / p.BH;
+    pair = pairs - 1 - b / p.BH;
     bh = b % p.BH;
   } else {
-    bh = b / p.n_qtiles;
-    qt = b % p.n_qtiles;
+    bh = b / pairs;
+    pair = b % pairs;
   }
-  const int row0 = qt * C::BF;
   const int bh_kv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
-  const int last_row = min(row0 + C::BF, p.M) - 1;
-  const int key_end = kCausal ? min(p.N, last_row + 1) : p.N;  // keys [0, key_end) are visible to some row
-  const int steps = (key_end + C::BS - 1) / C::BS;
+  int row0[C::kQT], steps[C::kQT];
+  int n_max = 0;
+#pragma unroll
+  for (int t = 0; t < C::kQT; ++t) {
+    row0[t] = (pair * C::kQT + t) * C::BF;
+    steps[t] = (dq_key_end<kCausal>(row0[t], p.M, p.N) + C::BS - 1) / C::BS;
+    n_max = max(n_max, steps[t]);
+  }
 
   if (threadIdx.x == 0) {
     misc[1] = 0u;
     misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
-    mbar_init(bar(Lay::kBarQ), 1);
+    for (int t = 0; t < C::kQT; ++t) {
+      mbar_init(bar(C::kBarQ + t), 1);
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 128);
+    }
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(Lay::kBarFull + s), 1);
-      mbar_init(bar(Lay::kBarEmpty + s), 1);
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(Lay::kBarSFull + s), 1);
-      mbar_init(bar(Lay::kBarPFull + s), 128);
-    }
-    mbar_init(bar(Lay::kBarDone), 1);
+    mbar_init(bar(C::kBarDone), 1);
     fence_mbar_init();
   }
   if (warp == C::kTmaWarp && lane == 0) {
@@ -520,7 +563,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     prefetch_tensormap(&tmV);
   }
   if (warp == C::kMmaWarp) {
-    tmem_alloc(base + Lay::kOffMisc, C::kTmemCols);
+    tmem_alloc(base + C::kOffMisc, C::kTmemCols);
     tmem_relinquish_alloc_permit();
   }
   tc_fence_before_sync();
@@ -534,104 +577,128 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_fix = l2_policy_evict_first();
       const uint64_t pol_str = l2_policy_evict_last();
-      mbar_arrive_expect_tx(bar(Lay::kBarQ), 2 * C::kFixTile);
 #pragma unroll
-      for (int cb = 0; cb < C::kColBlocks; ++cb) {
-        tma_load_3d_hint(base + Lay::kOffQ + cb * C::kFixBlock, &tmQ, bar(Lay::kBarQ), cb * 64, row0, bh, pol_fix);
-        tma_load_3d_hint(base + Lay::kOffDO + cb * C::kFixBlock, &tmdO, bar(Lay::kBarQ), cb * 64, row0, bh,
-                         pol_fix);
+      for (int t = 0; t < C::kQT; ++t) {
+        if (steps[t] == 0) continue;
+        mbar_arrive_expect_tx(bar(C::kBarQ + t), 2 * C::kFixTile);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb) {
+          tma_load_3d_hint(base + C::kOffQ + t * C::kFixTile + cb * C::kFixBlock, &tmQ, bar(C::kBarQ + t), cb * 64,
+                           row0[t], bh, pol_fix);
+          tma_load_3d_hint(base + C::kOffDO + t * C::kFixTile + cb * C::kFixBlock, &tmdO, bar(C::kBarQ + t),
+                           cb * 64, row0[t], bh, pol_fix);
+        }
       }
       int issued = 0;
-      for (int t = 0; t < steps; ++t) {
-        const int s = t % C::kStages;
-        const uint32_t use = static_cast<uint32_t>(t / C::kStages);
-        if (use > 0 && !FA2_BWD_WAIT(bar(Lay::kBarEmpty + s), (use - 1) & 1u, kStatusBwdTimeoutTma)) break;
-        const uint32_t fb = bar(Lay::kBarFull + s);
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t use = static_cast<uint32_t>(j / C::kStages);
+        if (use > 0 && !FA2_BWD_WAIT(bar(C::kBarEmpty + s), (use - 1) & 1u, kStatusBwdTimeoutTma)) break;
+        const uint32_t fb = bar(C::kBarFull + s);
         mbar_arrive_expect_tx(fb, 2 * C::kStrTile);
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb) {
-          tma_load_3d_hint(base + Lay::k_off(s) + cb * C::kStrBlock, &tmK, fb, cb * 64, t * C::BS, bh_kv, pol_str);
-          tma_load_3d_hint(base + Lay::v_off(s) + cb * C::kStrBlock, &tmV, fb, cb * 64, t * C::BS, bh_kv, pol_str);
+          tma_load_3d_hint(base + C::k_off(s) + cb * C::kStrBlock, &tmK, fb, cb * 64, j * C::BS, bh_kv, pol_str);
+          tma_load_3d_hint(base + C::v_off(s) + cb * C::kStrBlock, &tmV, fb, cb * 64, j * C::BS, bh_kv, pol_str);
         }
-        issued = t + 1;
+        issued = j + 1;
       }
       if (*wctx.abort_flag) {
-        drain_bounded(bar(Lay::kBarQ), 0);
-        for (int t = max(0, issued - C::kStages); t < issued; ++t)
-          drain_bounded(bar(Lay::kBarFull + t % C::kStages), (t / C::kStages) & 1);
+        for (int t = 0; t < C::kQT; ++t)
+          if (steps[t] > 0) drain_bounded(bar(C::kBarQ + t), 0);
+        for (int j = max(0, issued - C::kStages); j < issued; ++j)
+          drain_bounded(bar(C::kBarFull + j % C::kStages), (j / C::kStages) & 1);
       }
     }
     __syncwarp();
   } else if (!skip && warp == C::kMmaWarp) {
     if (lane == 0) {
-      bool ok = FA2_BWD_WAIT(bar(Lay::kBarQ), 0, kStatusBwdTimeoutMmaLoad);
-      for (int t = 0; ok && t <= steps; ++t) {
-        if (t < steps) {
-          const int s = t % C::kStages, ts = t % 2;
-          ok = FA2_BWD_WAIT(bar(Lay::kBarFull + s), (t / C::kStages) & 1, kStatusBwdTimeoutMmaLoad);
-          if (!ok) break;
-          tc_fence_after_sync();
-          // S = Q K^T and dP = dO V^T: M = 128 queries, N = 64 keys, K = D
+      bool ok = true;
 #pragma unroll
-          for (int kk = 0; kk < C::kStepsD; ++kk) {
-            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
-            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
-            mma_f16_ss(tmem + C::kColS(ts), smem_desc_sw128(base + Lay::kOffQ + fo, 16, 1024),
-                       smem_desc_sw128(base + Lay::k_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+      for (int t = 0; t < C::kQT; ++t)
+        if (ok && steps[t] > 0) ok = FA2_BWD_WAIT(bar(C::kBarQ + t), 0, kStatusBwdTimeoutMmaLoad);
+      for (int j = 0; ok && j <= n_max; ++j) {
+        const int s = j % C::kStages;
+        bool kv_ready = false;
+#pragma unroll
+        for (int t = 0; t < C::kQT; ++t) {
+          if (j >= 1 && j - 1 < steps[t]) {
+            // dQ_t += dS_t K_{j-1}: M = 128 queries, N = D, K = 64 keys; K tile MN-major
+            const int jp = j - 1, sp = jp % C::kStages;
+            ok = FA2_BWD_WAIT(bar(C::kBarPFull + t), jp & 1, kStatusBwdTimeoutMmaP);
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < C::BS / C::kMmaK; ++kk)
+              mma_f16_ts(tmem + C::kColQ(t), tmem + C::kColS(t) + kk * 8,
+                         smem_desc(base + C::k_off(sp) + kk * C::kMmaK * 128, C::kStrBlock, 1024, kLayoutSw128),
+                         C::kIdescAcc, (jp > 0 || kk > 0) ? 1u : 0u);
           }
+          if (j < steps[t]) {
+            if (!kv_ready) {
+              ok = FA2_BWD_WAIT(bar(C::kBarFull + s), (j / C::kStages) & 1, kStatusBwdTimeoutMmaLoad);
+              if (!ok) break;
+              kv_ready = true;
+              tc_fence_after_sync();
+            }
+            // S_t = Q_t K_j^T and dP_t = dO_t V_j^T: M = 128 queries, N = 64 keys, K = D
+            const uint32_t qb = base + C::kOffQ + t * C::kFixTile, ob = base + C::kOffDO + t * C::kFixTile;
 #pragma unroll
-          for (int kk = 0; kk < C::kStepsD; ++kk) {
-            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
-            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
-            mma_f16_ss(tmem + C::kColDP(ts), smem_desc_sw128(base + Lay::kOffDO + fo, 16, 1024),
-                       smem_desc_sw128(base + Lay::v_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < C::kStepsD; ++kk) {
+              const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
+              const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
+              mma_f16_ss(tmem + C::kColS(t), smem_desc_sw128(qb + fo, 16, 1024),
+                         smem_desc_sw128(base + C::k_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 0; kk < C::kStepsD; ++kk) {
+              const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
+              const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
+              mma_f16_ss(tmem + C::kColDP(t), smem_desc_sw128(ob + fo, 16, 1024),
+                         smem_desc_sw128(base + C::v_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bar(C::kBarSFull + t));
           }
-          tc_commit(bar(Lay::kBarSFull + ts));
         }
-        if (t >= 1) {
-          const int tp = t - 1, sp = tp % C::kStages, tsp = tp % 2;
-          ok = FA2_BWD_WAIT(bar(Lay::kBarPFull + tsp), (tp / 2) & 1, kStatusBwdTimeoutMmaP);
-          if (!ok) break;
-          tc_fence_after_sync();
-          // dQ += dS K: M = 128 queries, N = D, K = 64 keys; dS from TMEM, K tile MN-major
-#pragma unroll
-          for (int kk = 0; kk < C::BS / C::kMmaK; ++kk)
-            mma_f16_ts(tmem + C::kColAcc0, tmem + C::kColS(tsp) + kk * 8,
-                       smem_desc(base + Lay::k_off(sp) + kk * C::kMmaK * 128, C::kStrBlock, 1024, kLayoutSw128),
-                       C::kIdescAcc, (tp > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(Lay::kBarEmpty + sp));
-        }
+        if (!ok) break;
+        // a K/V stage is handed back after every GEMM reading it was issued
+        if (j >= 1) tc_commit(bar(C::kBarEmpty + (j - 1) % C::kStages));
       }
-      tc_commit(bar(Lay::kBarDone));
-      drain_bounded(bar(Lay::kBarDone), 0);
+      tc_commit(bar(C::kBarDone));
+      drain_bounded(bar(C::kBarDone), 0);
     }
     __syncwarp();
-  } else if (!skip && warp < 4) {
-    const int r = warp * 32 + lane;  // query row of the tile = TMEM lane
-    const int row = row0 + r;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const int64_t vec = static_cast<int64_t>(bh) * p.Mpad + row;  // row < Mpad always
-    const float l2 = p.lse2[vec];
-    const float dl = p.dlt[vec];
+  } else if (!skip && warp < C::kSoftWarps) {
+    const int t = warp / 4;
+    const int r = (warp % 4) * 32 + lane;  // query row of tile t = TMEM lane
+    const int tile_row0 = (pair * C::kQT + t) * C::BF;
+    const int row = tile_row0 + r;
+    const int n_t = (dq_key_end<kCausal>(tile_row0, p.M, p.N) + C::BS - 1) / C::BS;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    float l2 = INFINITY, dl = 0.f;
+    if (n_t > 0) {
+      const int64_t vec = static_cast<int64_t>(bh) * p.Mpad + row;  // row < Mpad when the tile is in range
+      l2 = p.lse2[vec];
+      dl = p.dlt[vec];
+    }
     const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int t = 0; t < steps; ++t) {
-      const int ts = t % 2;
-      ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarSFull + ts), (t / 2) & 1, kStatusBwdTimeoutSoftmax));
+    bool ok = n_t > 0;
+    for (int j = 0; ok && j < n_t; ++j) {
+      ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(C::kBarSFull + t), j & 1, kStatusBwdTimeoutSoftmax));
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t sv[64], dv[64];
-      tmem_ld_x32(tmem + lane_addr + C::kColS(ts), *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld_x32(tmem + lane_addr + C::kColS(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts), *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
-      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+      tmem_ld_x32(tmem + lane_addr + C::kColS(t), *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColS(t) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(t), *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(t) + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
       tmem_ld_wait();
       reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
       reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
       // keys past N (zero-filled rows of K) and, when causal, keys after this row
-      const int kbase = t * C::BS;
+      const int kbase = j * C::BS;
       int lim = p.N - 1 - kbase;
       if (kCausal) lim = min(lim, row - kbase);
       uint32_t dk[32];
@@ -645,43 +712,45 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
         dk[c / 2] = pack_bf16x2(d2[0], d2[1]);
       }
-      tmem_st_x32(tmem + lane_addr + C::kColS(ts), dk);
+      tmem_st_x32(tmem + lane_addr + C::kColS(t), dk);
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(bar(Lay::kBarPFull + ts));
+      mbar_arrive(bar(C::kBarPFull + t));
     }
-    if (ok) ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarDone), 0, kStatusBwdTimeoutEpilogue));
-    if (ok) {
-      tc_fence_after_sync();
-      const uint32_t stage = base + Lay::kOffQ;  // Q's tile is free once every MMA has completed
+    if (n_t > 0) {
+      if (ok) ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(C::kBarDone), 0, kStatusBwdTimeoutEpilogue));
+      const uint32_t stage = base + C::kOffQ + t * C::kFixTile;  // Q_t's tile, free once every MMA completed
+      if (ok) {
+        tc_fence_after_sync();
 #pragma unroll
-      for (int ch = 0; ch < C::D / 32; ++ch) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_addr + C::kColAcc0 + ch * 32, v);
-        tmem_ld_wait();
-        reg_fence_x32(v);
+        for (int ch = 0; ch < C::D / 32; ++ch) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_addr + C::kColQ(t) + ch * 32, v);
+          tmem_ld_wait();
+          reg_fence_x32(v);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int cidx = ch * 4 + q4;
-          const int cb = cidx / 8, c = cidx % 8;
-          const uint32_t addr = stage + cb * C::kFixBlock + r * 128 + ((c ^ (r & 7)) << 4);
-          uint32_t w[4];
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int cidx = ch * 4 + q4;
+            const int cb = cidx / 8, c = cidx % 8;
+            const uint32_t addr = stage + cb * C::kFixBlock + r * 128 + ((c ^ (r & 7)) << 4);
+            uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * p.scale,
-                               __uint_as_float(v[q4 * 8 + 2 * e + 1]) * p.scale);
-          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * p.scale,
+                                 __uint_as_float(v[q4 * 8 + 2 * e + 1]) * p.scale);
+            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          }
         }
       }
-    }
-    fence_proxy_async_smem();
-    named_barrier_sync(1, 128);
-    if (r == 0 && ok && *wctx.abort_flag == 0u) {
+      fence_proxy_async_smem();
+      named_barrier_sync(1 + t, 128);
+      if (r == 0 && ok && *wctx.abort_flag == 0u) {
 #pragma unroll
-      for (int cb = 0; cb < C::kColBlocks; ++cb)
-        tma_store_3d(&tmdQ, base + Lay::kOffQ + cb * C::kFixBlock, cb * 64, row0, bh);
-      tma_store_commit();
-      tma_store_wait_read_all();
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_store_3d(&tmdQ, stage + cb * C::kFixBlock, cb * 64, tile_row0, bh);
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
     }
   }
 
