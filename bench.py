@@ -394,7 +394,7 @@ def run_ours(args, rank, local, world):
                             softcap=w.softcap, alibi_slopes=slopes, num_splits=1, stream=stream)
     elif w.split_kv:
         dcode = fa2.FA2_BF16 if w.dtype == si.BF16 else fa2.FA2_FP32
-        n_split = fa2.fa2_splitkv_num_splits(w.B, w.H, w.M, w.N, w.D, dcode)
+        n_split = fa2.fa2_splitkv_num_splits(w.B, w.H, w.Hkv, w.M, w.N, w.D, dcode)
         ws = torch.empty(max(256, fa2.fa2_splitkv_workspace_bytes(w.B, w.H, w.M, w.D, n_split)),
                          dtype=torch.uint8, device=dev)
         launches_per_step = 2 if n_split > 1 else 1  # forward slices + combine

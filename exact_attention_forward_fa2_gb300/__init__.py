@@ -49,7 +49,7 @@ SIGNATURES = {
     "fa2_bwd_workspace_bytes": ([_I, _I, _I], _SZ),
     "fa2_fwd_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                       _I, _VP], _I),
-    "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I], _I),
+    "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "fa2_strerror": ([_I], ctypes.c_char_p),
     "fa2_device_status": ([_I, ctypes.POINTER(_I)], _I),
@@ -140,9 +140,9 @@ def _stream_handle(q, stream):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def fa2_splitkv_num_splits(B: int, H: int, M: int, N: int, D: int, dtype: int) -> int:
+def fa2_splitkv_num_splits(B: int, H: int, H_kv: int, M: int, N: int, D: int, dtype: int) -> int:
     """Split count chosen by the library for the current device."""
-    rc = lib().fa2_splitkv_num_splits(B, H, M, N, D, dtype)
+    rc = lib().fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype)
     if rc < 0:
         raise Fa2Error(rc, "fa2_splitkv_num_splits")
     return rc
@@ -168,7 +168,7 @@ def fa2_fwd_splitkv(q, k, v, o=None, lse=None, scale: float | None = None, causa
         scale = 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
         if num_splits <= 0:
-            num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype)
+            num_splits = fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype)
         need = fa2_splitkv_workspace_bytes(B, H, M, D, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -215,7 +215,7 @@ def fa2_fwd_ext(q, k, v, o=None, lse=None, scale: float | None = None, causal: b
     wl, wr = (int(x) for x in window)
     with torch.cuda.device(q.device):
         if num_splits <= 0:
-            num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype)
+            num_splits = fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype)
         need = fa2_splitkv_workspace_bytes(B, H, M, D, num_splits)
         if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

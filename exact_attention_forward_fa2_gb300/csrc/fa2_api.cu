@@ -104,6 +104,17 @@ constexpr int kMaxSplits = 64;
 
 int64_t kv_tiles_total(int N) { return (static_cast<int64_t>(N) + 127) / 128; }
 
+// Whether a unit pairs the single query tile of two heads that read the same
+// key/value head (two tile slots per CTA, M <= 128, an even number of query
+// heads per key/value head) instead of two query tiles of one head.
+bool pair_heads(int H, int H_kv, int M, int qt) { return qt == 2 && M <= 128 && (H / H_kv) % 2 == 0; }
+
+// CTAs of the forward before any key split.
+int64_t forward_units(int B, int H, int H_kv, int M, int qt) {
+  if (pair_heads(H, H_kv, M, qt)) return static_cast<int64_t>(B) * H / 2;
+  return static_cast<int64_t>(B) * H * ((static_cast<int64_t>(M) + qt * 128 - 1) / (qt * 128));
+}
+
 // Split count that fills about one wave of CTAs when the query tiles alone do
 // not: floor(#SMs / units), with at least 4 key tiles per split.
 int auto_splits(int64_t units, int N, int sms) {
@@ -158,7 +169,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   const int64_t bh = static_cast<int64_t>(B) * H;
   const int64_t bh_kv = static_cast<int64_t>(B) * H_kv;
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
-  const int64_t units = bh * ((static_cast<int64_t>(M) + qt * 128 - 1) / (qt * 128));
+  const int64_t units = forward_units(B, H, H_kv, M, qt);
   if (bh > INT_MAX || units > INT_MAX) return FA2_ERR_TOO_LARGE;
   const int64_t n_kv = kv_tiles_total(N);
   int tiles_per_split = static_cast<int>(n_kv);
@@ -203,6 +214,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
                                                    lpart_offset(rows, D, num_splits))
                         : nullptr;
   L.params.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  L.params.pair_heads = pair_heads(H, H_kv, M, qt) ? 1 : 0;
   // window bounds: an absent side widens to cover every key (row - M <= 0 and
   // row + N >= N - 1 for every row); causal caps the right side at the diagonal
   L.params.win_left = (mods.window_left < 0 || mods.window_left > M) ? M : mods.window_left;
@@ -280,17 +292,16 @@ extern "C" int fa2_fwd_gqa(const void* q, const void* k, const void* v, void* o,
                      stream);
 }
 
-extern "C" int fa2_splitkv_num_splits(int B, int H, int M, int N, int D, int dtype) {
+extern "C" int fa2_splitkv_num_splits(int B, int H, int H_kv, int M, int N, int D, int dtype) {
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
+  if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
   if (D != 64 && D != 128) return FA2_ERR_HEADDIM;
   if (dtype != FA2_BF16 && dtype != FA2_FP32) return FA2_ERR_DTYPE;
   int sms = 0;
   const int rc = sm_count(&sms);
   if (rc != FA2_OK) return rc;
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
-  const int64_t units =
-      static_cast<int64_t>(B) * H * ((static_cast<int64_t>(M) + qt * 128 - 1) / (qt * 128));
-  return auto_splits(units, N, sms);
+  return auto_splits(forward_units(B, H, H_kv, M, qt), N, sms);
 }
 
 extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits) {
@@ -303,7 +314,7 @@ extern "C" int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void
                                int causal, int dtype, int num_splits, void* workspace,
                                size_t workspace_size, void* stream) {
   if (num_splits <= 0) {
-    num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype);
+    num_splits = fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype);
     if (num_splits < 0) return num_splits;
   }
   if (num_splits > kMaxSplits) num_splits = kMaxSplits;
@@ -317,7 +328,7 @@ extern "C" int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o,
                            const float* alibi_slopes, int alibi_batch_stride, int dtype,
                            int num_splits, void* workspace, size_t workspace_size, void* stream) {
   if (num_splits <= 0) {
-    num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype);
+    num_splits = fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype);
     if (num_splits < 0) return num_splits;
   }
   if (num_splits > kMaxSplits) num_splits = kMaxSplits;

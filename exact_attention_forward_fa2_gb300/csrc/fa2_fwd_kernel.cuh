@@ -54,6 +54,10 @@ struct FwdParams {
   int tiles_per_split;
   float* o_part;        // [num_splits][BH][M][D] fp32 (num_splits > 1)
   float* l_part;        // [num_splits][BH][M] fp32 (num_splits > 1)
+  // 1: a unit is the single query tile of two heads that read the same key/value
+  // head (M <= 128 under grouped-query attention), instead of two query tiles of one
+  // head, so that both tile slots of a CTA work and share the streamed K/V tiles
+  int pair_heads;
   // score modifiers, read by the kMod instantiations only: key j is visible to
   // query row i iff i - win_left <= j <= i + win_right (the host folds the causal
   // bound into win_right and widens an unbounded side to cover every key);
@@ -163,6 +167,11 @@ struct Unit {
 // keep one head's query tiles adjacent so its K/V stay hot in L2.
 __device__ __forceinline__ Unit unit_of_block(const FwdParams& p, bool causal, int b) {
   Unit u;
+  if (p.pair_heads) {  // every unit is one tile long: any order
+    u.bh = 2 * b;
+    u.pair = 0;
+    return u;
+  }
   if (causal) {
     u.pair = p.units_per_head - 1 - b / p.BH;
     u.bh = b % p.BH;
@@ -180,6 +189,14 @@ __device__ __forceinline__ int kv_tiles_for(int row0, int M, int N, bool causal)
   if (!causal) return total;
   const int last_row = min(row0 + 128, M) - 1;
   return min(total, last_row / 128 + 1);
+}
+
+// Query tile t of a unit: its flat head and first row.
+__device__ __forceinline__ int tile_head(const FwdParams& p, const Unit& u, int t) {
+  return u.bh + (p.pair_heads ? t : 0);
+}
+__device__ __forceinline__ int tile_first_row(const FwdParams& p, const Unit& u, int t, int tiles_per_unit) {
+  return (u.pair * tiles_per_unit + (p.pair_heads ? 0 : t)) * 128;
 }
 
 // Key tiles [first, first + count) that the query tile starting at row0 visits
@@ -259,7 +276,7 @@ __device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity) {
 // row sums the same way.
 template <class C, bool kCausal, bool kMod>
 __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtensorMap& tmO, Unit unit,
-                                               int split, int kb, int bh, uint32_t base, uint32_t tmem,
+                                               int split, int kb, uint32_t base, uint32_t tmem,
                                                int warp, int lane, const WaitCtx& wctx) {
   using namespace ptx;
   constexpr int kC = C::BN / 2;  // score columns (keys) of this thread
@@ -269,7 +286,8 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
   const int t = g % C::kQTiles;
   const int h = g / C::kQTiles;
   const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
-  const int tile_row0 = (unit.pair * C::kQTiles + t) * C::BM;
+  const int tile_row0 = tile_first_row(p, unit, t, C::kQTiles);
+  const int bh_t = tile_head(p, unit, t);
   const int row = tile_row0 + r;
   const KvSpan span = kv_span<kMod>(tile_row0, p, kCausal, split);
   const int n_t = span.count;
@@ -297,7 +315,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
   float slope_s = 0.f;
   if constexpr (kMod) {
     if (p.alibi != nullptr) {
-      const float a = p.alibi[(bh / p.H) * p.alibi_bstride + bh % p.H];
+      const float a = p.alibi[(bh_t / p.H) * p.alibi_bstride + bh_t % p.H];
       slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
     }
   }
@@ -434,7 +452,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
       float lo_sum = 0.f;
       if (n_t > 0 && ok) ok = __all_sync(0xffffffffu, exchange(l_run, lo_sum));
       const float l_tot = l_run + lo_sum;
-      const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh) * p.M + row;
+      const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh_t) * p.M + row;
       float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D + h * kOC);
       if (n_t > 0 && ok) {
         tc_fence_after_sync();
@@ -471,7 +489,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
 #pragma unroll
       for (int cidx = h * kChunks / 2; cidx < (h + 1) * kChunks / 2; ++cidx)
         st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
-      if (row < p.M && h == 0) p.lse[static_cast<int64_t>(bh) * p.M + row] = -INFINITY;
+      if (row < p.M && h == 0) p.lse[static_cast<int64_t>(bh_t) * p.M + row] = -INFINITY;
     } else if (ok) {
       tc_fence_after_sync();
       const float inv_l = l_tot > 0.f ? 1.0f / l_tot : 0.f;
@@ -507,14 +525,14 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
         }
       }
       if (row < p.M && h == 0)
-        p.lse[static_cast<int64_t>(bh) * p.M + row] = (m_run + lg2_approx(l_tot)) * 0.69314718055994530942f;
+        p.lse[static_cast<int64_t>(bh_t) * p.M + row] = (m_run + lg2_approx(l_tot)) * 0.69314718055994530942f;
     }
     fence_proxy_async_smem();
     named_barrier_sync(1 + t, 256);
     if (r == 0 && h == 0 && *wctx.abort_flag == 0u) {
 #pragma unroll
       for (int cb = 0; cb < C::kColBlocks; ++cb)
-        tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh);
+        tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh_t);
       tma_store_commit();
       tma_store_wait_read_all();
     }
@@ -553,7 +571,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   int ks = kb, n_max = 0;
 #pragma unroll
   for (int t = 0; t < C::kQTiles; ++t) {
-    row0[t] = (unit.pair * C::kQTiles + t) * C::BM;
+    row0[t] = tile_first_row(p, unit, t, C::kQTiles);
     const KvSpan sp = kv_span<kMod>(row0[t], p, kCausal, split);
     kt0[t] = sp.first;
     nkv[t] = sp.count;
@@ -633,7 +651,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ,
-                           bar(C::kBarQ + t), cb * C::kSwElems, row0[t], bh, pol_q);
+                           bar(C::kBarQ + t), cb * C::kSwElems, row0[t], tile_head(p, unit, t), pol_q);
       }
       int issued = 0;  // K/V tiles whose loads were issued
       for (int j = 0; j < n_max; ++j) {
@@ -753,12 +771,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     __syncwarp();
   } else if (!skip && warp < C::kSoftmaxWarps && C::kHalves == 2) {
-    softmax_halves<C, kCausal, kMod>(p, tmO, unit, split, kb, bh, base, tmem, warp, lane, wctx);
+    softmax_halves<C, kCausal, kMod>(p, tmO, unit, split, kb, base, tmem, warp, lane, wctx);
   } else if (!skip && warp < C::kSoftmaxWarps) {
     // ---------------------------------------------------------- softmax warpgroups
     const int t = warp / 4;
     const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
-    const int tile_row0 = (unit.pair * C::kQTiles + t) * C::BM;
+    const int tile_row0 = tile_first_row(p, unit, t, C::kQTiles);
+    const int bh_t = tile_head(p, unit, t);
     const int row = tile_row0 + r;
     const KvSpan span = kv_span<kMod>(tile_row0, p, kCausal, split);
     const int n_t = span.count;
@@ -773,7 +792,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     float slope_s = 0.f;  // ALiBi slope of this head, in the units S is held in
     if constexpr (kMod) {
       if (p.alibi != nullptr) {
-        const float a = p.alibi[(bh / p.H) * p.alibi_bstride + bh % p.H];
+        const float a = p.alibi[(bh_t / p.H) * p.alibi_bstride + bh_t % p.H];
         slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
       }
     }
@@ -948,7 +967,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (n_t > 0 && ok)
           ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
                                                     kStatusTimeoutEpilogue));
-        const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh) * p.M + row;
+        const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh_t) * p.M + row;
         float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D);
         if (n_t > 0 && ok) {
           tc_fence_after_sync();
@@ -989,7 +1008,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
         for (int cidx = 0; cidx < C::kColBlocks * 8; ++cidx)
           st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
-        if (row < p.M) p.lse[static_cast<int64_t>(bh) * p.M + row] = -INFINITY;
+        if (row < p.M) p.lse[static_cast<int64_t>(bh_t) * p.M + row] = -INFINITY;
       } else if (ok) {
         tc_fence_after_sync();
         l_run = row_sum();
@@ -1028,7 +1047,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (row < p.M) {
           // L = ln(2) * (m + log2 l): the base-2 running state converted to natural log
           const float L = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
-          p.lse[static_cast<int64_t>(bh) * p.M + row] = L;
+          p.lse[static_cast<int64_t>(bh_t) * p.M + row] = L;
         }
       }
       fence_proxy_async_smem();
@@ -1036,7 +1055,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       if (r == 0 && *wctx.abort_flag == 0u) {
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh);
+          tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh_t);
         tma_store_commit();
         tma_store_wait_read_all();
       }

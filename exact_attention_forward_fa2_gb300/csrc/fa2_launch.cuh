@@ -37,8 +37,13 @@ cudaError_t launch_cfg(FwdLaunch& L) {
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  L.params.units_per_head = (L.params.M + C::kQTiles * C::BM - 1) / (C::kQTiles * C::BM);
-  L.params.num_units = L.params.units_per_head * L.params.BH;
+  if (L.params.pair_heads) {  // one tile of each of two heads per unit
+    L.params.units_per_head = 1;
+    L.params.num_units = L.params.BH / 2;
+  } else {
+    L.params.units_per_head = (L.params.M + C::kQTiles * C::BM - 1) / (C::kQTiles * C::BM);
+    L.params.num_units = L.params.units_per_head * L.params.BH;
+  }
   bool* done = attr_done[dev];
   if (L.mod && L.params.cap_in > 0.f)
     return L.causal ? launch_one<CH, true, true>(L, done[5]) : launch_one<CH, false, true>(L, done[4]);

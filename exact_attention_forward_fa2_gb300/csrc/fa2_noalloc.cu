@@ -50,7 +50,7 @@ extern "C" int fa2_fwd_splitkv_noalloc(const void* q, const void* k, const void*
                                        float scale, int causal, int dtype, int num_splits,
                                        void* stream) {
   if (num_splits <= 0) {
-    num_splits = fa2_splitkv_num_splits(B, H, M, N, D, dtype);
+    num_splits = fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype);
     if (num_splits < 0) return num_splits;
   }
   // The partials must fit in the built-in buffer; refuse rather than overflow it.

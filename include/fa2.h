@@ -113,9 +113,10 @@ int fa2_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float*
                     int num_splits, void* workspace, size_t workspace_size, void* stream);
 
 /* Split count fa2_fwd_splitkv uses when given num_splits <= 0, for the current
- * device (about one wave of CTAs, at least 4 key tiles per slice); >= 1, or a
+ * device (about one wave of CTAs, at least 4 key tiles per slice; H_kv counts
+ * because a CTA serves two query heads of a group when M <= 128); >= 1, or a
  * negative FA2_ERR_* code for invalid sizes or when the device cannot be queried. */
-int fa2_splitkv_num_splits(int B, int H, int M, int N, int D, int dtype);
+int fa2_splitkv_num_splits(int B, int H, int H_kv, int M, int N, int D, int dtype);
 
 /* Workspace bytes fa2_fwd_splitkv needs for num_splits slices (0 if num_splits <= 1
  * or the sizes are invalid): num_splits * B*H*M * (D + 1) * 4 plus padding. */

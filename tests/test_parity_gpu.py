@@ -199,10 +199,40 @@ def test_split_kv_all_rows(fa2, shape, causal, dtype):
     v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
     tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
     # a workspace full of NaN: every value the combine reads must have been written
-    ns = splits if splits > 0 else fa2.fa2_splitkv_num_splits(B, H, M, N, D, 0 if dtype == si.BF16 else 1)
+    ns = splits if splits > 0 else fa2.fa2_splitkv_num_splits(B, H, Hkv, M, N, D, 0 if dtype == si.BF16 else 1)
     nbytes = max(256, fa2.fa2_splitkv_workspace_bytes(B, H, M, D, ns))
     ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device=DEV).view(torch.uint8)
     o, lse = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=D ** -0.5, causal=causal, num_splits=ns, workspace=ws)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, D ** -0.5, causal)
+    eo, el, excess = compare(to_host_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, l_ref, dtype)
+    assert excess <= 0 and el <= TOL[dtype], (eo, el)
+
+
+PAIRED = [  # (B, H, H_kv, M, N, D, num_splits): M <= 128 and an even group, so a CTA
+    # serves one query tile of two heads that share a key/value head
+    (2, 8, 2, 128, 700, 128, 1),
+    (1, 4, 1, 77, 300, 64, 1),       # ragged M, multi-query
+    (2, 16, 4, 100, 2000, 128, 0),   # with the library's split count
+    (1, 8, 4, 128, 1500, 64, 5),
+    (1, 6, 2, 128, 400, 128, 1),     # odd group (3): not paired, same answer
+]
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", PAIRED, ids=lambda s: "x".join(map(str, s)))
+def test_paired_heads_all_rows(fa2, shape, causal, dtype):
+    B, H, Hkv, M, N, D, splits = shape
+    seed = 3500 + sum(shape)
+    q = si.normal(seed, 1, (B, H, M, D), 1.0, dtype)
+    k = si.normal(seed, 2, (B, Hkv, N, D), 1.0, dtype)
+    v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    if splits == 1:
+        o, lse = fa2.fa2_fwd(tq, tk, tv, scale=D ** -0.5, causal=causal)
+    else:
+        o, lse = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=D ** -0.5, causal=causal, num_splits=splits)
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, D ** -0.5, causal)
     eo, el, excess = compare(to_host_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, l_ref, dtype)

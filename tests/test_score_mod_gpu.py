@@ -93,6 +93,8 @@ CASES = [  # (B, H, Hkv, M, N, D, causal, window, softcap, slopes)
     (2, 2, 2, 200, 333, 64, False, (-1, -1), 0.0, "bh"),        # ALiBi per (b, h), both sides
     (1, 4, 1, 390, 520, 128, True, (150, -1), 4.0, "h"),        # all three, MQA
     (2, 2, 2, 129, 1100, 64, False, (300, 40), 2.5, "bh"),      # all three
+    (2, 8, 2, 128, 900, 128, True, (300, -1), 0.0, "bh"),       # paired heads (M <= 128, group 4)
+    (1, 8, 4, 96, 700, 64, False, (200, 100), 3.0, "h"),        # paired heads with softcap
 ]
 
 
