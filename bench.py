@@ -456,7 +456,19 @@ def run_ours(args, rank, local, world):
         # TF32 contraction: the measured bf16 peak times the nominal dense TF32/BF16 ratio
         peak = peak * TF32_OVER_BF16
         peak_kind = f"tf32 = {TF32_OVER_BF16:.3f} x {peak_kind} (nominal 1.1/2.25 PFLOP/s)"
-    achieved = flops / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e12
+    launch_s = sum(kernel_ms) / len(kernel_ms) / 1e3
+    achieved = flops / launch_s / 1e12
+    io = w.io_bytes()
+    # below the ridge (peak FLOP/s over peak HBM bytes/s) the launch is bound by
+    # reading Q, K, V and writing O, L once: decode-shaped workloads
+    hbm_bound = (not bwd) and flops / io < peak * 1e12 / (hbm_peak * 1e9)
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": io / launch_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "frac": io / launch_s / 1e9 / hbm_peak, "peak_kind": "HBM copy, measured",
+                "tensor_tflops": achieved, "tensor_peak_tflops": peak}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_kind": peak_kind}
     line = {
         "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps,
@@ -470,9 +482,8 @@ def run_ours(args, rank, local, world):
                    **({"num_splits": n_split} if w.split_kv else {}),
                    **({"window": list(w.window), "softcap": w.softcap, "alibi": w.alibi}
                       if w.modified else {})},
-        "frac_of_peak": achieved / peak,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
+        "frac_of_peak": roof["frac"],
+        "roofline": {**roof,
                      "traffic": dram_traffic_per_launch(w.name, args.pass_),
                      "kernel": "fa2_bwd (preprocess + dK/dV + dQ kernels)" if bwd else KERNEL,
                      "algorithmic_flops_per_launch": flops,

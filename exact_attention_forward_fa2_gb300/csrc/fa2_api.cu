@@ -109,6 +109,16 @@ int64_t kv_tiles_total(int N) { return (static_cast<int64_t>(N) + 127) / 128; }
 // heads per key/value head) instead of two query tiles of one head.
 bool pair_heads(int H, int H_kv, int M, int qt) { return qt == 2 && M <= 128 && (H / H_kv) % 2 == 0; }
 
+// Whether the query heads of each key/value head are computed as the rows of one
+// problem with H_kv heads of (H / H_kv) * M rows.  Under grouped-query attention
+// the heads of a group are contiguous in q, o and lse and read the same K and V,
+// so without a causal mask or score modifiers that problem is the same attention
+// computed on the same memory; with few query rows (decode) it fills 128-row
+// tiles that would otherwise hold M rows each.
+bool pack_heads(int H, int H_kv, int M, int causal, bool use_mod) {
+  return !use_mod && !causal && H / H_kv >= 2 && M < 128;
+}
+
 // CTAs of the forward before any key split.
 int64_t forward_units(int B, int H, int H_kv, int M, int qt) {
   if (pair_heads(H, H_kv, M, qt)) return static_cast<int64_t>(B) * H / 2;
@@ -166,6 +176,11 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
                        mods.softcap > 0.f || mods.alibi != nullptr;
   // the kernel forms row +- window and key - row in 32-bit ints and fp32
   if (use_mod && (M > (1 << 30) || N > (1 << 30))) return FA2_ERR_TOO_LARGE;
+  // packed heads: the same memory seen as H_kv heads of (H / H_kv) * M rows
+  if (pack_heads(H, H_kv, M, causal, use_mod)) {
+    M = (H / H_kv) * M;
+    H = H_kv;
+  }
   const int64_t bh = static_cast<int64_t>(B) * H;
   const int64_t bh_kv = static_cast<int64_t>(B) * H_kv;
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
@@ -301,6 +316,12 @@ extern "C" int fa2_splitkv_num_splits(int B, int H, int H_kv, int M, int N, int 
   const int rc = sm_count(&sms);
   if (rc != FA2_OK) return rc;
   const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
+  // the CTAs of the forward as it will run (heads packed under the non-causal
+  // rule; a causal problem, never packed, only gets more CTAs)
+  if (pack_heads(H, H_kv, M, 0, false)) {
+    M = (H / H_kv) * M;
+    H = H_kv;
+  }
   return auto_splits(forward_units(B, H, H_kv, M, qt), N, sms);
 }
 

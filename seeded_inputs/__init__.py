@@ -175,6 +175,10 @@ WORKLOADS = {
     # cache): 32 query-tile units cannot fill the GPU, so the key range is split
     "bf16_1x32x128x32768x128_gqa8_splitkv": Workload("bf16_1x32x128x32768x128_gqa8_splitkv", 1, 32, 128, 32768, 128,
                                                      BF16, False, 7, H_kv=8, split_kv=True),
+    # decode: one query row per sequence against an 8192-key cache, grouped-query
+    # heads; bound by reading K and V once from HBM
+    "bf16_16x32x1x8192x128_gqa8_decode": Workload("bf16_16x32x1x8192x128_gqa8_decode", 16, 32, 1, 8192, 128, BF16,
+                                                  False, 11, H_kv=8, split_kv=True),
     # score modifiers at the headline size: a 2048-key causal sliding window, a
     # softcap of 50, ALiBi with the geometric slopes below
     "bf16_2x16x8192x8192x128_causal_window2048": Workload("bf16_2x16x8192x8192x128_causal_window2048", 2, 16, 8192,

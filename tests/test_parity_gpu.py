@@ -209,6 +209,38 @@ def test_split_kv_all_rows(fa2, shape, causal, dtype):
     assert excess <= 0 and el <= TOL[dtype], (eo, el)
 
 
+PACKED = [  # (B, H, H_kv, M, N, D, num_splits, causal): grouped-query attention with few
+    # query rows; without a causal mask the group's heads are computed as the rows
+    # of one taller problem (causal cases run unpacked: same answer expected)
+    (4, 32, 8, 1, 3000, 128, 0, False),    # decode: 8 rows per key/value head
+    (2, 8, 2, 3, 500, 64, 1, False),       # 12 rows
+    (2, 16, 4, 16, 700, 128, 3, False),    # 64 rows, key split
+    (1, 16, 2, 16, 1000, 128, 1, False),   # exactly 128 rows
+    (1, 16, 2, 40, 600, 64, 1, False),     # 320 rows over three tiles
+    (2, 16, 4, 16, 700, 128, 3, True),     # causal: not packed
+    (2, 4, 1, 127, 260, 128, 0, False),    # multi-query, 508 rows
+]
+
+
+@pytest.mark.parametrize("dtype", [si.BF16, si.FP32])
+@pytest.mark.parametrize("shape", PACKED, ids=lambda s: "x".join(map(str, s)))
+def test_packed_heads_all_rows(fa2, shape, dtype):
+    B, H, Hkv, M, N, D, splits, causal = shape
+    seed = 3700 + sum(int(x) for x in shape)
+    q = si.normal(seed, 1, (B, H, M, D), 1.0, dtype)
+    k = si.normal(seed, 2, (B, Hkv, N, D), 1.0, dtype)
+    v = si.normal(seed, 3, (B, Hkv, N, D), 1.0, dtype)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    if splits == 1:
+        o, lse = fa2.fa2_fwd(tq, tk, tv, scale=D ** -0.5, causal=causal)
+    else:
+        o, lse = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=D ** -0.5, causal=causal, num_splits=splits)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, D ** -0.5, causal)
+    eo, el, excess = compare(to_host_f64(o), lse.cpu().numpy().astype(np.float64), o_ref, l_ref, dtype)
+    assert excess <= 0 and el <= TOL[dtype], (eo, el)
+
+
 PAIRED = [  # (B, H, H_kv, M, N, D, num_splits): M <= 128 and an even group, so a CTA
     # serves one query tile of two heads that share a key/value head
     (2, 8, 2, 128, 700, 128, 1),
@@ -278,7 +310,7 @@ def full_or_sampled(fa2, name, sampled):
 
 @pytest.mark.parametrize("name", ["fp32_1x1x128x128x64", "tf32_4x12x2048x2048x64",
                                   "bf16_4x16x4096x4096x64_causal", "bf16_8x32x1000x3000x128_sharp",
-                                  "bf16_1x32x128x32768x128_gqa8_splitkv"])
+                                  "bf16_1x32x128x32768x128_gqa8_splitkv", "bf16_16x32x1x8192x128_gqa8_decode"])
 def test_workload_full(fa2, name):
     full_or_sampled(fa2, name, sampled=False)
 
