@@ -40,6 +40,7 @@ WORKLOAD = "bf16_2x16x8192x8192x128_causal"
 METRIC = "FA2 fwd TFLOP/s (4BHMND, 1/2 causal) and % of GB300 dense tensor peak"
 METRIC_BWD = "FA2 bwd TFLOP/s (10BHMND, 1/2 causal) and % of GB300 dense tensor peak"
 BWD_FLOPS_OVER_FWD = 2.5
+REFERENCE_BUDGET_S = 120.0  # CPU seconds of oracle work for a whole --impl reference run
 UNIT = "TFLOP/s"
 KERNEL = "fa2_fwd_kernel"
 def profile_summary(workload: str, pass_: str = "fwd") -> str:
@@ -211,8 +212,9 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
-    """Time the fp64 oracle on a bounded, seeded sample of the workload's rows.
+def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0, n_start: int = 64):
+    """Time the fp64 oracle on a bounded, seeded sample of the workload's rows,
+    growing the sample from ``n_start`` rows until it takes ``seconds_target``.
     Returns (TFLOP/s, rows, seconds, cores)."""
     import oracle
     rng = np.random.default_rng(seed)
@@ -228,7 +230,7 @@ def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0):
 
     rows = np.sort(rng.choice(total_rows, size=64, replace=False))
     run(rows[:8])  # warm (build, pages)
-    n = 64
+    n = max(8, min(total_rows, n_start))
     while True:
         rows = np.sort(rng.choice(total_rows, size=n, replace=False))
         t0 = time.perf_counter()
@@ -277,10 +279,17 @@ def run_reference(args, rank, world):
     w = si.WORKLOADS[args.workload]
     q, k, v = si.make_qkv(w)
     bwd = args.pass_ == "bwd"
+    # each step is a bounded sample, sized so that the whole run stays near
+    # REFERENCE_BUDGET_S of CPU work (at most 2 s per step)
+    per_step_s = max(0.05, min(2.0, REFERENCE_BUDGET_S / (args.warmup + args.steps)))
     per_step = []
+    n_rows = 64
     for step in range(args.warmup + args.steps):
-        sample = oracle_sample_bwd if bwd else oracle_sample
-        tf, n, dt, cores = sample(w, q, k, v, seconds_target=2.0, seed=step)
+        if bwd:
+            tf, n, dt, cores = oracle_sample_bwd(w, q, k, v, seconds_target=per_step_s, seed=step)
+        else:  # start each step's sample at the size the previous step reached
+            tf, n, dt, cores = oracle_sample(w, q, k, v, seconds_target=per_step_s, seed=step, n_start=n_rows)
+            n_rows = n
         if step >= args.warmup:
             per_step.append((tf, n, dt))
     value = float(np.mean([p[0] for p in per_step]))
@@ -294,9 +303,10 @@ def run_reference(args, rank, world):
                    "N": w.N, "D": w.D, "causal": w.causal},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": (f"per step: {per_step[-1][1]} whole query heads of the workload "
-                                    f"(fp64 backward), ~2 s of CPU work" if bwd else
+                                    f"(fp64 backward), >= {per_step_s:.2f} s of CPU work" if bwd else
                                     f"per step: {per_step[-1][1]} seeded random query rows of the "
-                                    f"workload (fp64, all their visible keys), ~2 s of CPU work")},
+                                    f"workload (fp64, all their visible keys), ~{per_step_s:.2f} s of "
+                                    f"CPU work")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
