@@ -51,6 +51,7 @@ SIGNATURES = {
                       _I, _VP], _I),
     "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I, _I], _I),
     "fa2_splitkv_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "fa2_selftest_wait_timeout": ([_I, _VP], _I),
     "fa2_strerror": ([_I], ctypes.c_char_p),
     "fa2_device_status": ([_I, ctypes.POINTER(_I)], _I),
     "fa2_version": ([], _I),
@@ -99,6 +100,17 @@ def fa2_device_status(reset: bool = True) -> int:
     if rc not in (FA2_OK, FA2_ERR_DEVICE_TIMEOUT):
         raise Fa2Error(rc, "fa2_device_status")
     return raw.value
+
+
+def fa2_selftest_wait_timeout(limit_ms: int = 20, stream=None) -> None:
+    """Run the failure-path self-test (C ABI ``fa2_selftest_wait_timeout``): a
+    bounded wait that runs out after ``limit_ms`` and sets the device status word
+    to 99.  Read and clear it with fa2_device_status()."""
+    import torch
+    handle = _stream_handle(torch.empty(0, device="cuda"), stream)
+    rc = lib().fa2_selftest_wait_timeout(int(limit_ms), handle)
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_selftest_wait_timeout")
 
 
 def _check_qkv(q, k, v):

@@ -545,4 +545,30 @@ extern "C" int fa2_device_status(int reset, int* raw_code) {
   return word == 0 ? FA2_OK : FA2_ERR_DEVICE_TIMEOUT;
 }
 
+// Self-test of the failure path: one thread waits, through the kernels' own
+// bounded wait, on an mbarrier phase that nothing completes, gives up after
+// limit_ns and records kStatusSelfTest in the device status word, exactly as a
+// pipeline wait of a real kernel that ran out would.
+__global__ void fa2_selftest_wait_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0u;
+    fa2::ptx::mbar_init(fa2::ptx::smem_u32(&bar), 1);
+    fa2::ptx::fence_mbar_init();
+    const fa2::WaitCtx w{&abort_flag, status};
+    (void)fa2::wait_bounded(fa2::ptx::smem_u32(&bar), 0, w, fa2::kStatusSelfTest, limit_ns);
+  }
+}
+
+extern "C" int fa2_selftest_wait_timeout(int limit_ms, void* stream) {
+  if (limit_ms < 1 || limit_ms > 2000) return FA2_ERR_SHAPE;
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != FA2_OK) return rc;
+  fa2_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      st->status, static_cast<uint64_t>(limit_ms) * 1000000ull);
+  return cudaGetLastError() == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
 extern "C" int fa2_version(void) { return 200; }

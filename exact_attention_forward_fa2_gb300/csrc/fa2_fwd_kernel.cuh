@@ -83,6 +83,7 @@ enum : int {
   kStatusTimeoutSoftmaxO = 8,
   kStatusTimeoutEpilogue = 9,
   kStatusTimeoutSoftmaxX = 10,  // the two halves of a score row exchanging max or sum
+  kStatusSelfTest = 99,         // fa2_selftest_wait_timeout: a wait that was meant to run out
 };
 
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s; a real wait lasts microseconds
@@ -244,14 +245,14 @@ struct WaitCtx {
 
 // Bounded mbarrier wait.  False if the CTA is aborting or the wait ran out.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w,
-                                             int code) {
+                                             int code, uint64_t limit_ns = kWaitTimeoutNs) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*w.abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      if (ptx::globaltimer_ns() - t0 > limit_ns) {
         *w.abort_flag = 1u;
         atomicCAS(w.status, 0, code);
         return false;

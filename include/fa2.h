@@ -255,6 +255,18 @@ const char* fa2_strerror(int status);
  */
 int fa2_device_status(int reset, int* raw_code);
 
+/*
+ * fa2_selftest_wait_timeout -- exercises the failure path.  Launches one thread
+ * on `stream` that waits, with the same bounded wait every pipeline wait of the
+ * kernels uses, on a barrier that nothing completes; after limit_ms (1..2000) it
+ * gives up and records code 99 in the device status word, as a kernel whose
+ * pipeline stalled would.  Nothing hangs and the context stays usable: later
+ * launches see the word and return without computing until fa2_device_status
+ * clears it.  A test hook; the pages have no counterpart.  Returns FA2_OK when
+ * launched, FA2_ERR_SHAPE for limit_ms out of range.
+ */
+int fa2_selftest_wait_timeout(int limit_ms, void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fa2_version(void);
 

@@ -33,8 +33,9 @@ def lib():
 def test_header_declares_the_api():
     assert declared_functions() == ["fa2_bwd", "fa2_bwd_workspace_bytes", "fa2_device_status", "fa2_fwd",
                                     "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_host", "fa2_fwd_splitkv",
-                                    "fa2_fwd_splitkv_noalloc", "fa2_splitkv_num_splits",
-                                    "fa2_splitkv_workspace_bytes", "fa2_strerror", "fa2_version"]
+                                    "fa2_fwd_splitkv_noalloc", "fa2_selftest_wait_timeout",
+                                    "fa2_splitkv_num_splits", "fa2_splitkv_workspace_bytes", "fa2_strerror",
+                                    "fa2_version"]
 
 
 def test_exports_every_declared_symbol(lib):
@@ -197,6 +198,11 @@ def call_host(lib, **kw):
 ])
 def test_host_entry_rejects_bad_arguments(lib, kw, code):
     assert call_host(lib, **kw) == code
+
+
+@pytest.mark.parametrize("limit", [0, -5, 2001])
+def test_selftest_rejects_limits_out_of_range(lib, limit):
+    assert lib.fa2_selftest_wait_timeout(limit, None) == fa2.FA2_ERR_SHAPE
 
 
 def test_no_gpu_means_an_error_not_a_fallback(lib):
