@@ -692,6 +692,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (!skip && warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // Descriptor words of the operand tiles.  The low word holds the start
+      // address >> 4, so a K step or another ring stage is one 32-bit add to it;
+      // fewer instructions between MMAs keep the tensor core's queue fed while
+      // the softmax warps share this warp's scheduler.
+      const uint64_t qk_desc = smem_desc_sw128(base, 16, 1024);
+      const uint32_t qk_lo0 = static_cast<uint32_t>(qk_desc), qk_hi = static_cast<uint32_t>(qk_desc >> 32);
+      const uint64_t v_desc = C::kBF16 ? smem_desc(base + C::kOffV, C::kBlockBytes, 1024, kLayoutSw128)
+                                       : smem_desc(base + C::kOffV, C::kBlockBytes, 512, kLayoutSw128Atom32);
+      const uint32_t v_lo0 = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < C::kQTiles; ++t)
@@ -705,22 +714,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             // O_t += P_t V_{j-1}
             const int jp = j - 1;
             const int sv = jp % C::kStages;
-            ok = wait_bounded(bar(C::kBarPFull + t), (kMod ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
-            if (!ok) break;
+            // V first: it has normally landed long ago, and checking it while P is
+            // still being written keeps that check off the path from P to the MMAs
             if (!v_ready) {
               ok = wait_bounded(bar(C::kBarVFull + sv), (jp / C::kStages) & 1, wctx, kStatusTimeoutMmaV);
               if (!ok) break;
               v_ready = true;
             }
+            ok = wait_bounded(bar(C::kBarPFull + t), (kMod ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
+            if (!ok) break;
             tc_fence_after_sync();
-            const uint32_t v_base = base + C::kOffV + sv * C::kVTileBytes;
+            const uint32_t v_lo = v_lo0 + static_cast<uint32_t>(sv) * (C::kVTileBytes >> 4);
             const int jp0 = kMod ? jb[t] : 0;  // first P V of this tile overwrites O
 #pragma unroll
             for (int kk = 0; kk < C::kStepsPV; ++kk) {
               // B = V rows [kk*kMmaK, +kMmaK), all D columns, MN-major
-              const uint64_t bdesc =
-                  C::kBF16 ? smem_desc(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 1024, kLayoutSw128)
-                           : smem_desc(v_base + kk * C::kMmaK * 128, C::kBlockBytes, 512, kLayoutSw128Atom32);
+              const uint64_t bdesc = desc_from_words(v_lo + (kk * C::kMmaK * 128 >> 4), v_hi);
               const uint32_t a_tmem = tmem + C::kColS(t) + kk * 8;
               if constexpr (C::kBF16)
                 mma_f16_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
@@ -737,13 +746,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               k_ready = true;
               tc_fence_after_sync();
             }
-            const uint32_t q_base = base + C::kOffQ + t * C::kTileBytes;
-            const uint32_t k_base = base + C::kOffK + s * C::kTileBytes;
+            const uint32_t q_lo = qk_lo0 + ((C::kOffQ + t * C::kTileBytes) >> 4);
+            const uint32_t k_lo = qk_lo0 + ((C::kOffK >> 4) + static_cast<uint32_t>(s) * (C::kTileBytes >> 4));
 #pragma unroll
             for (int kk = 0; kk < C::kStepsS; ++kk) {
-              const uint32_t off = (kk / 4) * C::kBlockBytes + (kk % 4) * 32;
-              const uint64_t adesc = smem_desc_sw128(q_base + off, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(k_base + off, 16, 1024);
+              const uint32_t off = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
+              const uint64_t adesc = desc_from_words(q_lo + off, qk_hi);
+              const uint64_t bdesc = desc_from_words(k_lo + off, qk_hi);
               if constexpr (C::kBF16)
                 mma_f16_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
               else

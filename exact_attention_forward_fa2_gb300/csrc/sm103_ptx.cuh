@@ -233,6 +233,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t smem_addr, uint32_t lbo_b
   return d;
 }
 
+// A descriptor from its two 32-bit words.  The low word is (start address >> 4)
+// | (leading byte offset >> 4) << 16; shared-memory addresses of a CTA stay below
+// 256 KB, so adding a 16-byte-multiple offset >> 4 to it moves the start address
+// without touching the other fields.
+__device__ __forceinline__ uint64_t desc_from_words(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr, uint32_t lbo_bytes,
                                                     uint32_t sbo_bytes) {
   return smem_desc(smem_addr, lbo_bytes, sbo_bytes, kLayoutSw128);
