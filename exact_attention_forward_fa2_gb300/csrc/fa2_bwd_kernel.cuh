@@ -280,6 +280,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
   } else if (!skip && warp == C::kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
+      // Descriptor words (K-major operands; MN-major B of the accumulating GEMMs):
+      // a K step or a ring stage is one add to the low word, which keeps the
+      // instructions between MMAs few (the issuing thread shares its scheduler
+      // with the P/dS warps).
+      const uint64_t dk = smem_desc_sw128(base, 16, 1024);
+      const uint64_t dm = smem_desc(base, C::kStrBlock, 1024, kLayoutSw128);
+      const uint32_t k_lo0 = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+      const uint32_t m_lo0 = static_cast<uint32_t>(dm), m_hi = static_cast<uint32_t>(dm >> 32);
       bool ok = FA2_BWD_WAIT(bar(Lay::kBarKV), 0, kStatusBwdTimeoutMmaLoad);
       for (int t = 0; ok && t <= u.steps; ++t) {
         if (t < u.steps) {
@@ -287,20 +295,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           ok = FA2_BWD_WAIT(bar(Lay::kBarFull + s), (t / C::kStages) & 1, kStatusBwdTimeoutMmaLoad);
           if (!ok) break;
           tc_fence_after_sync();
+          const uint32_t q_lo = k_lo0 + (static_cast<uint32_t>(Lay::q_off(s)) >> 4);
+          const uint32_t do_lo = k_lo0 + (static_cast<uint32_t>(Lay::do_off(s)) >> 4);
           // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 64 queries, K = D
 #pragma unroll
           for (int kk = 0; kk < C::kStepsD; ++kk) {
-            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
-            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
-            mma_f16_ss(tmem + C::kColS(ts), smem_desc_sw128(base + Lay::kOffK + fo, 16, 1024),
-                       smem_desc_sw128(base + Lay::q_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+            const uint32_t fo = ((kk / 4) * C::kFixBlock + (kk % 4) * 32) >> 4;
+            const uint32_t so = ((kk / 4) * C::kStrBlock + (kk % 4) * 32) >> 4;
+            mma_f16_ss(tmem + C::kColS(ts), desc_from_words(k_lo0 + (Lay::kOffK >> 4) + fo, k_hi),
+                       desc_from_words(q_lo + so, k_hi), C::kIdescS, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < C::kStepsD; ++kk) {
-            const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
-            const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
-            mma_f16_ss(tmem + C::kColDP(ts), smem_desc_sw128(base + Lay::kOffV + fo, 16, 1024),
-                       smem_desc_sw128(base + Lay::do_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+            const uint32_t fo = ((kk / 4) * C::kFixBlock + (kk % 4) * 32) >> 4;
+            const uint32_t so = ((kk / 4) * C::kStrBlock + (kk % 4) * 32) >> 4;
+            mma_f16_ss(tmem + C::kColDP(ts), desc_from_words(k_lo0 + (Lay::kOffV >> 4) + fo, k_hi),
+                       desc_from_words(do_lo + so, k_hi), C::kIdescS, kk > 0 ? 1u : 0u);
           }
           tc_commit(bar(Lay::kBarSFull + ts));
         }
@@ -309,17 +319,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           ok = FA2_BWD_WAIT(bar(Lay::kBarPFull + tsp), (tp / 2) & 1, kStatusBwdTimeoutMmaP);
           if (!ok) break;
           tc_fence_after_sync();
+          const uint32_t q_lo = m_lo0 + (static_cast<uint32_t>(Lay::q_off(sp)) >> 4);
+          const uint32_t do_lo = m_lo0 + (static_cast<uint32_t>(Lay::do_off(sp)) >> 4);
           // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, K = 64 queries;
           // A from TMEM (packed bf16), B = the 64-row tile read MN-major
 #pragma unroll
           for (int kk = 0; kk < C::BS / C::kMmaK; ++kk) {
-            const uint32_t bo = kk * C::kMmaK * 128;
-            mma_f16_ts(tmem + C::kColAcc0, tmem + C::kColS(tsp) + kk * 8,
-                       smem_desc(base + Lay::do_off(sp) + bo, C::kStrBlock, 1024, kLayoutSw128), C::kIdescAcc,
-                       (tp > 0 || kk > 0) ? 1u : 0u);
-            mma_f16_ts(tmem + C::kColAcc1, tmem + C::kColDP(tsp) + kk * 8,
-                       smem_desc(base + Lay::q_off(sp) + bo, C::kStrBlock, 1024, kLayoutSw128), C::kIdescAcc,
-                       (tp > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t bo = (kk * C::kMmaK * 128) >> 4;
+            mma_f16_ts(tmem + C::kColAcc0, tmem + C::kColS(tsp) + kk * 8, desc_from_words(do_lo + bo, m_hi),
+                       C::kIdescAcc, (tp > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ts(tmem + C::kColAcc1, tmem + C::kColDP(tsp) + kk * 8, desc_from_words(q_lo + bo, m_hi),
+                       C::kIdescAcc, (tp > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar(Lay::kBarEmpty + sp));
         }
@@ -613,6 +623,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     __syncwarp();
   } else if (!skip && warp == C::kMmaWarp) {
     if (lane == 0) {
+      // descriptor words, as in the dK/dV issuer
+      const uint64_t dk = smem_desc_sw128(base, 16, 1024);
+      const uint64_t dm = smem_desc(base, C::kStrBlock, 1024, kLayoutSw128);
+      const uint32_t k_lo0 = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+      const uint32_t m_lo0 = static_cast<uint32_t>(dm), m_hi = static_cast<uint32_t>(dm >> 32);
       bool ok = true;
 #pragma unroll
       for (int t = 0; t < C::kQT; ++t)
@@ -628,11 +643,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ok = FA2_BWD_WAIT(bar(C::kBarPFull + t), jp & 1, kStatusBwdTimeoutMmaP);
             if (!ok) break;
             tc_fence_after_sync();
+            const uint32_t kv_lo = m_lo0 + (static_cast<uint32_t>(C::k_off(sp)) >> 4);
 #pragma unroll
             for (int kk = 0; kk < C::BS / C::kMmaK; ++kk)
               mma_f16_ts(tmem + C::kColQ(t), tmem + C::kColS(t) + kk * 8,
-                         smem_desc(base + C::k_off(sp) + kk * C::kMmaK * 128, C::kStrBlock, 1024, kLayoutSw128),
-                         C::kIdescAcc, (jp > 0 || kk > 0) ? 1u : 0u);
+                         desc_from_words(kv_lo + ((kk * C::kMmaK * 128) >> 4), m_hi), C::kIdescAcc,
+                         (jp > 0 || kk > 0) ? 1u : 0u);
           }
           if (j < steps[t]) {
             if (!kv_ready) {
@@ -642,20 +658,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               tc_fence_after_sync();
             }
             // S_t = Q_t K_j^T and dP_t = dO_t V_j^T: M = 128 queries, N = 64 keys, K = D
-            const uint32_t qb = base + C::kOffQ + t * C::kFixTile, ob = base + C::kOffDO + t * C::kFixTile;
+            const uint32_t q_lo = k_lo0 + ((C::kOffQ + t * C::kFixTile) >> 4);
+            const uint32_t o_lo = k_lo0 + ((C::kOffDO + t * C::kFixTile) >> 4);
+            const uint32_t kk_lo = k_lo0 + (static_cast<uint32_t>(C::k_off(s)) >> 4);
+            const uint32_t vv_lo = k_lo0 + (static_cast<uint32_t>(C::v_off(s)) >> 4);
 #pragma unroll
             for (int kk = 0; kk < C::kStepsD; ++kk) {
-              const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
-              const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
-              mma_f16_ss(tmem + C::kColS(t), smem_desc_sw128(qb + fo, 16, 1024),
-                         smem_desc_sw128(base + C::k_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+              const uint32_t fo = ((kk / 4) * C::kFixBlock + (kk % 4) * 32) >> 4;
+              const uint32_t so = ((kk / 4) * C::kStrBlock + (kk % 4) * 32) >> 4;
+              mma_f16_ss(tmem + C::kColS(t), desc_from_words(q_lo + fo, k_hi), desc_from_words(kk_lo + so, k_hi),
+                         C::kIdescS, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
             for (int kk = 0; kk < C::kStepsD; ++kk) {
-              const uint32_t fo = (kk / 4) * C::kFixBlock + (kk % 4) * 32;
-              const uint32_t so = (kk / 4) * C::kStrBlock + (kk % 4) * 32;
-              mma_f16_ss(tmem + C::kColDP(t), smem_desc_sw128(ob + fo, 16, 1024),
-                         smem_desc_sw128(base + C::v_off(s) + so, 16, 1024), C::kIdescS, kk > 0 ? 1u : 0u);
+              const uint32_t fo = ((kk / 4) * C::kFixBlock + (kk % 4) * 32) >> 4;
+              const uint32_t so = ((kk / 4) * C::kStrBlock + (kk % 4) * 32) >> 4;
+              mma_f16_ss(tmem + C::kColDP(t), desc_from_words(o_lo + fo, k_hi), desc_from_words(vv_lo + so, k_hi),
+                         C::kIdescS, kk > 0 ? 1u : 0u);
             }
             tc_commit(bar(C::kBarSFull + t));
           }
