@@ -80,7 +80,7 @@ enum : int {
   kStatusTimeoutMmaV = 5,
   kStatusTimeoutMmaP = 6,
   kStatusTimeoutSoftmaxS = 7,
-  kStatusTimeoutSoftmaxO = 8,
+  // 8 is retired: the O rescale needs no wait of its own (P_{j-1} V_{j-1} completed before S_j)
   kStatusTimeoutEpilogue = 9,
   kStatusTimeoutSoftmaxX = 10,  // the two halves of a score row exchanging max or sum
   kStatusSelfTest = 99,         // fa2_selftest_wait_timeout: a wait that was meant to run out
@@ -130,7 +130,7 @@ struct FwdCfg {
   static constexpr int kOffK = kOffQ + kQTiles * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kStages * kVTileBytes;
-  static constexpr int kNumBars = 4 * kQTiles + 4 * kStages + 1 + (kHalves == 2 ? kQTiles : 0);
+  static constexpr int kNumBars = 4 * kQTiles + 3 * kStages + 1 + (kHalves == 2 ? kQTiles : 0);
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   // exchange buffer of the two halves: [2 parities][kQTiles][2 halves][128 rows] floats
   static constexpr int kOffX = kOffMisc + 16;
@@ -139,10 +139,9 @@ struct FwdCfg {
   // barrier indices
   static constexpr int kBarQ = 0;
   static constexpr int kBarKFull = kBarQ + kQTiles;
-  static constexpr int kBarKEmpty = kBarKFull + kStages;
-  static constexpr int kBarVFull = kBarKEmpty + kStages;
-  static constexpr int kBarVEmpty = kBarVFull + kStages;
-  static constexpr int kBarSFull = kBarVEmpty + kStages;
+  static constexpr int kBarFree = kBarKFull + kStages;
+  static constexpr int kBarVFull = kBarFree + kStages;
+  static constexpr int kBarSFull = kBarVFull + kStages;
   static constexpr int kBarPFull = kBarSFull + kQTiles;
   static constexpr int kBarOFull = kBarPFull + kQTiles;
   static constexpr int kBarMmaDone = kBarOFull + kQTiles;
@@ -425,8 +424,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
     unpack_f32x2(acc[3], a6, a7);
     l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
     if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (j - 1) & 1, wctx, kStatusTimeoutSoftmaxO));
-      if (!ok) break;
+      // P_{j-1} V_{j-1} completed before S_j, which this thread waited for
       tc_fence_after_sync();
 #pragma unroll
       for (int ch = 0; ch < kOC / 32; ++ch) {
@@ -449,7 +447,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
   if (p.num_splits > 1) {
     if (tile_row0 < p.M) {
       if (n_t > 0 && ok)
-        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx, kStatusTimeoutEpilogue));
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx, kStatusTimeoutEpilogue));
       float lo_sum = 0.f;
       if (n_t > 0 && ok) ok = __all_sync(0xffffffffu, exchange(l_run, lo_sum));
       const float l_tot = l_run + lo_sum;
@@ -480,7 +478,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
     }
   } else if (n_t > 0 || (kMod && tile_row0 < p.M)) {
     if (ok)
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx, kStatusTimeoutEpilogue));
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx, kStatusTimeoutEpilogue));
     float lo_sum = 0.f;
     if (ok) ok = __all_sync(0xffffffffu, exchange(l_run, lo_sum));
     const float l_tot = l_run + lo_sum;
@@ -606,9 +604,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
-      mbar_init(bar(C::kBarKEmpty + s), 1);
+      mbar_init(bar(C::kBarFree + s), 1);
       mbar_init(bar(C::kBarVFull + s), 1);
-      mbar_init(bar(C::kBarVEmpty + s), 1);
     }
     mbar_init(bar(C::kBarMmaDone), 1);
     fence_mbar_init();
@@ -658,14 +655,18 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       for (int j = 0; j < n_max; ++j) {
         const int s = j % C::kStages;
         const uint32_t use = static_cast<uint32_t>(j / C::kStages);
-        if (use > 0 && !wait_bounded(bar(C::kBarKEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaK))
+        // K_j replaces K_{j-S}, free after MMA round j-S; V_j replaces V_{j-S}, free
+        // after round j-S+1 (which ran P V on it).  One barrier per round.
+        if (use > 0 && !wait_bounded(bar(C::kBarFree + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaK))
           break;
         mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < C::kColBlocks; ++cb)
           tma_load_3d_hint(base + C::kOffK + s * C::kTileBytes + cb * C::kBlockBytes, &tmK,
                            bar(C::kBarKFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
-        if (use > 0 && !wait_bounded(bar(C::kBarVEmpty + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaV)) {
+        if (use > 0 && !wait_bounded(bar(C::kBarFree + (j - C::kStages + 1) % C::kStages),
+                                     static_cast<uint32_t>((j - C::kStages + 1) / C::kStages) & 1u, wctx,
+                                     kStatusTimeoutTmaV)) {
           issued = -(j + 1);  // K_j issued, V_j not
           break;
         }
@@ -736,7 +737,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               else
                 mma_tf32_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
             }
-            tc_commit(bar(C::kBarOFull + t));
+            // O_t is read by the epilogue after its last P V; a rescale on the way
+            // needs no barrier of its own (it follows S_{jp+1}, issued after this)
+            if (jp == jb[t] + nkv[t] - 1) tc_commit(bar(C::kBarOFull + t));
           }
           if ((kMod ? j >= jb[t] : true) && j < jb[t] + nkv[t]) {
             // S_t = Q_t K_j^T
@@ -772,8 +775,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
           if (!ok) break;
         }
-        if (j >= 1) tc_commit(bar(C::kBarVEmpty + (j - 1) % C::kStages));
-        if (j < n_max) tc_commit(bar(C::kBarKEmpty + s));
+        // Round j's commit frees K_j (read by this round's S GEMMs) and V_{j-1}
+        // (read by its P V GEMMs); the loader waits for round i - kStages before
+        // loading K_i and for round i - kStages + 1 before loading V_i.
+        if (j < n_max) tc_commit(bar(C::kBarFree + s));
       }
       // every MMA issued above must finish before TMEM is released
       tc_commit(bar(C::kBarMmaDone));
@@ -925,10 +930,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
       }
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O_t *= alpha once P_{j-1} V_{j-1} has landed in TMEM
-        ok = __all_sync(0xffffffffu,
-                        wait_bounded(bar(C::kBarOFull + t), (j - 1) & 1, wctx, kStatusTimeoutSoftmaxO));
-        if (!ok) break;
+        // O_t *= alpha.  P_{j-1} V_{j-1} has landed: the MMA warp issued it before
+        // S_j, and a commit completes only after every earlier MMA.
         tc_fence_after_sync();
 #pragma unroll
         for (int ch = 0; ch < C::D / 32; ++ch) {
@@ -975,7 +978,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // log); a split without visible keys for the tile contributes O_s = 0, L_s = -inf
       if (tile_row0 < p.M) {
         if (n_t > 0 && ok)
-          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
+          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx,
                                                     kStatusTimeoutEpilogue));
         const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh_t) * p.M + row;
         float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D);
@@ -1010,7 +1013,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // (kMod: a window can leave every row of a tile without a visible key; the
       // tile is then written as O = 0, L = -inf)
       if (ok)
-        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), (n_t - 1) & 1, wctx,
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx,
                                                   kStatusTimeoutEpilogue));
       // Q_t's shared tile is free once the last GEMM of this tile completed: stage O there
       const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
