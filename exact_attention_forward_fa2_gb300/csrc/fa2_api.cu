@@ -240,7 +240,8 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   L.params.alibi = mods.alibi;
   L.params.alibi_bstride = mods.alibi_bstride;
   L.causal = causal ? 1 : 0;
-  L.mod = use_mod ? 1 : 0;
+  L.win = (mods.window_left >= 0 || (!causal && mods.window_right >= 0)) ? 1 : 0;
+  L.mod = (mods.softcap > 0.f || mods.alibi != nullptr || L.win) ? 1 : 0;
   L.stream = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;

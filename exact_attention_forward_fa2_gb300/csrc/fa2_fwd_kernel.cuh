@@ -58,11 +58,12 @@ struct FwdParams {
   // head (M <= 128 under grouped-query attention), instead of two query tiles of one
   // head, so that both tile slots of a CTA work and share the streamed K/V tiles
   int pair_heads;
-  // score modifiers, read by the kMod instantiations only: key j is visible to
-  // query row i iff i - win_left <= j <= i + win_right (the host folds the causal
-  // bound into win_right and widens an unbounded side to cover every key);
-  // s <- cap_out * tanh(s * cap_in) in log2 units when cap_in > 0 (softcap);
-  // s <- s - log2(e) * slope * |i - j| when alibi is not null (ALiBi)
+  // score modifiers.  Window (read by the kWin instantiations): key j is visible
+  // to query row i iff i - win_left <= j <= i + win_right (the host folds the
+  // causal bound into win_right and widens an unbounded side to cover every key).
+  // Read by the kMod instantiations: s <- cap_out * tanh(s * cap_in) in log2 units
+  // when cap_in > 0 (softcap); s <- s - log2(e) * slope * |i - j| when alibi is
+  // not null (ALiBi)
   int win_left, win_right;
   float cap_in;         // scale / softcap, 0 = no softcap
   float cap_out;        // softcap * log2(e)
@@ -202,16 +203,16 @@ __device__ __forceinline__ int tile_first_row(const FwdParams& p, const Unit& u,
 // Key tiles [first, first + count) that the query tile starting at row0 visits
 // inside split `split` (key tiles [split*tps, +tps)); count 0 = nothing to do.
 // Plain: every key tile, or up to the diagonal when causal; the first is the
-// split's first tile.  kMod: the tiles holding keys [row0 - win_left,
+// split's first tile.  kWin: the tiles holding keys [row0 - win_left,
 // last row + win_right] (a sliding window; the causal bound is in win_right).
 struct KvSpan {
   int first, count;
 };
 
-template <bool kMod>
+template <bool kWin>
 __device__ __forceinline__ KvSpan kv_span(int row0, const FwdParams& p, bool causal, int split) {
   const int s0 = split * p.tiles_per_split;
-  if constexpr (!kMod) {
+  if constexpr (!kWin) {
     const int n = kv_tiles_for(row0, p.M, p.N, causal) - s0;
     return KvSpan{s0, max(0, min(n, p.tiles_per_split))};
   } else {
@@ -274,7 +275,7 @@ __device__ __forceinline__ void drain_bounded(uint32_t bar, uint32_t parity) {
 // partial row maxima (shared memory + an mbarrier per tile), so P of one row is
 // scaled consistently for the P V product; at the end they add their partial
 // row sums the same way.
-template <class C, bool kCausal, bool kMod>
+template <class C, bool kCausal, bool kMod, bool kWin>
 __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtensorMap& tmO, Unit unit,
                                                int split, int kb, uint32_t base, uint32_t tmem,
                                                int warp, int lane, const WaitCtx& wctx) {
@@ -289,7 +290,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
   const int tile_row0 = tile_first_row(p, unit, t, C::kQTiles);
   const int bh_t = tile_head(p, unit, t);
   const int row = tile_row0 + r;
-  const KvSpan span = kv_span<kMod>(tile_row0, p, kCausal, split);
+  const KvSpan span = kv_span<kWin>(tile_row0, p, kCausal, split);
   const int n_t = span.count;
   const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
   const uint32_t tS = tmem + lane_addr + C::kColS(t) + h * kC;              // S of this half
@@ -337,7 +338,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
     float s[kC];
 #pragma unroll
     for (int c = 0; c < kC; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
-    const int key0 = ((kMod ? span.first : kb) + j) * C::BN;
+    const int key0 = ((kWin ? span.first : kb) + j) * C::BN;
     const int keyh = key0 + h * kC;  // key of this thread's column 0
     if constexpr (kMod) {
       if (capped) {
@@ -349,6 +350,8 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
 #pragma unroll
         for (int c = 0; c < kC; ++c) s[c] = fmaf(-slope_s, fabsf(d0 + static_cast<float>(c)), s[c]);
       }
+    }
+    if constexpr (kWin) {
       const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||
                             (key0 < tile_row0 + C::BM - 1 - p.win_left);
       if (boundary) {
@@ -476,7 +479,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
         if (h == 0) p.l_part[prow] = -INFINITY;
       }
     }
-  } else if (n_t > 0 || (kMod && tile_row0 < p.M)) {
+  } else if (n_t > 0 || (kWin && tile_row0 < p.M)) {
     if (ok)
       ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx, kStatusTimeoutEpilogue));
     float lo_sum = 0.f;
@@ -484,7 +487,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
     const float l_tot = l_run + lo_sum;
     const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
     constexpr int kChunks = C::kColBlocks * 8;  // 16-byte chunks of one O row
-    if (kMod && n_t == 0) {
+    if (kWin && n_t == 0) {
 #pragma unroll
       for (int cidx = h * kChunks / 2; cidx < (h + 1) * kChunks / 2; ++cidx)
         st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
@@ -538,7 +541,7 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
   }
 }
 
-template <class C, bool kCausal, bool kMod>
+template <class C, bool kCausal, bool kMod, bool kWin>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -571,13 +574,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
   for (int t = 0; t < C::kQTiles; ++t) {
     row0[t] = tile_first_row(p, unit, t, C::kQTiles);
-    const KvSpan sp = kv_span<kMod>(row0[t], p, kCausal, split);
+    const KvSpan sp = kv_span<kWin>(row0[t], p, kCausal, split);
     kt0[t] = sp.first;
     nkv[t] = sp.count;
     jb[t] = 0;
     n_max = max(n_max, nkv[t]);
   }
-  if constexpr (kMod) {
+  if constexpr (kWin) {
     int lo = 0x7fffffff, hi = 0;
 #pragma unroll
     for (int t = 0; t < C::kQTiles; ++t)
@@ -711,7 +714,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         bool v_ready = false, k_ready = false;
 #pragma unroll
         for (int t = 0; t < C::kQTiles; ++t) {
-          if ((kMod ? j - 1 >= jb[t] : j >= 1) && j - 1 < jb[t] + nkv[t]) {
+          if ((kWin ? j - 1 >= jb[t] : j >= 1) && j - 1 < jb[t] + nkv[t]) {
             // O_t += P_t V_{j-1}
             const int jp = j - 1;
             const int sv = jp % C::kStages;
@@ -722,11 +725,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
               if (!ok) break;
               v_ready = true;
             }
-            ok = wait_bounded(bar(C::kBarPFull + t), (kMod ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
+            ok = wait_bounded(bar(C::kBarPFull + t), (kWin ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
             if (!ok) break;
             tc_fence_after_sync();
             const uint32_t v_lo = v_lo0 + static_cast<uint32_t>(sv) * (C::kVTileBytes >> 4);
-            const int jp0 = kMod ? jb[t] : 0;  // first P V of this tile overwrites O
+            const int jp0 = kWin ? jb[t] : 0;  // first P V of this tile overwrites O
 #pragma unroll
             for (int kk = 0; kk < C::kStepsPV; ++kk) {
               // B = V rows [kk*kMmaK, +kMmaK), all D columns, MN-major
@@ -741,7 +744,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             // needs no barrier of its own (it follows S_{jp+1}, issued after this)
             if (jp == jb[t] + nkv[t] - 1) tc_commit(bar(C::kBarOFull + t));
           }
-          if ((kMod ? j >= jb[t] : true) && j < jb[t] + nkv[t]) {
+          if ((kWin ? j >= jb[t] : true) && j < jb[t] + nkv[t]) {
             // S_t = Q_t K_j^T
             if (!k_ready) {
               ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
@@ -765,7 +768,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           }
         }
         if (!ok) break;
-        if constexpr (kMod) {
+        if constexpr (kWin) {
           // a ring slot is handed back only after its copy landed, even if no
           // query tile of this CTA read it
           if (j >= 1 && !v_ready)
@@ -786,7 +789,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
     __syncwarp();
   } else if (!skip && warp < C::kSoftmaxWarps && C::kHalves == 2) {
-    softmax_halves<C, kCausal, kMod>(p, tmO, unit, split, kb, base, tmem, warp, lane, wctx);
+    softmax_halves<C, kCausal, kMod, kWin>(p, tmO, unit, split, kb, base, tmem, warp, lane, wctx);
   } else if (!skip && warp < C::kSoftmaxWarps) {
     // ---------------------------------------------------------- softmax warpgroups
     const int t = warp / 4;
@@ -794,7 +797,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int tile_row0 = tile_first_row(p, unit, t, C::kQTiles);
     const int bh_t = tile_head(p, unit, t);
     const int row = tile_row0 + r;
-    const KvSpan span = kv_span<kMod>(tile_row0, p, kCausal, split);
+    const KvSpan span = kv_span<kWin>(tile_row0, p, kCausal, split);
     const int n_t = span.count;
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_addr + C::kColS(t);
@@ -830,7 +833,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       float s[C::BN];
 #pragma unroll
       for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
-      const int key0 = ((kMod ? span.first : kb) + j) * C::BN;
+      const int key0 = ((kWin ? span.first : kb) + j) * C::BN;
       if constexpr (kMod) {
         // score modifiers: softcap (into log2 units), then the ALiBi distance penalty
         if (capped) {
@@ -842,6 +845,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::BN; ++c) s[c] = fmaf(-slope_s, fabsf(d0 + static_cast<float>(c)), s[c]);
         }
+      }
+      if constexpr (kWin) {
         // window mask, on tiles that cross N or either window edge of some row
         const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||
                               (key0 < tile_row0 + C::BM - 1 - p.win_left);
@@ -1009,15 +1014,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           p.l_part[prow] = -INFINITY;
         }
       }
-    } else if (n_t > 0 || (kMod && tile_row0 < p.M)) {
-      // (kMod: a window can leave every row of a tile without a visible key; the
+    } else if (n_t > 0 || (kWin && tile_row0 < p.M)) {
+      // (kWin: a window can leave every row of a tile without a visible key; the
       // tile is then written as O = 0, L = -inf)
       if (ok)
         ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx,
                                                   kStatusTimeoutEpilogue));
       // Q_t's shared tile is free once the last GEMM of this tile completed: stage O there
       const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
-      if (kMod && n_t == 0) {
+      if (kWin && n_t == 0) {
 #pragma unroll
         for (int cidx = 0; cidx < C::kColBlocks * 8; ++cidx)
           st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
@@ -1089,7 +1094,8 @@ struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmO;
   FwdParams params;
   int causal;
-  int mod;  // score modifiers in use (window, softcap or ALiBi): the kMod kernels
+  int mod;  // softcap or ALiBi in use: the kernels with kMod
+  int win;  // a sliding window in use: the kernels with kWin (spans and masks)
   cudaStream_t stream;
 };
 

@@ -8,10 +8,10 @@ namespace fa2 {
 
 // Sets the dynamic shared-memory limit once per device and kernel, then launches
 // one CTA per (work unit, key split) on the caller's stream.
-template <class C, bool kCausal, bool kMod>
+template <class C, bool kCausal, bool kMod, bool kWin>
 cudaError_t launch_one(FwdLaunch& L, bool& attr_done) {
   if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(fa2_fwd_kernel<C, kCausal, kMod>,
+    const cudaError_t e = cudaFuncSetAttribute(fa2_fwd_kernel<C, kCausal, kMod, kWin>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -19,8 +19,8 @@ cudaError_t launch_one(FwdLaunch& L, bool& attr_done) {
   }
   const dim3 grid(static_cast<unsigned>(L.params.num_units * L.params.num_splits));
   const dim3 block(C::kThreads);
-  fa2_fwd_kernel<C, kCausal, kMod><<<grid, block, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV,
-                                                                            L.tmO, L.params);
+  fa2_fwd_kernel<C, kCausal, kMod, kWin><<<grid, block, C::kSmemBytes, L.stream>>>(L.tmQ, L.tmK, L.tmV,
+                                                                                  L.tmO, L.params);
   return cudaGetLastError();
 }
 
@@ -32,7 +32,7 @@ cudaError_t launch_one(FwdLaunch& L, bool& attr_done) {
 template <class C>
 cudaError_t launch_cfg(FwdLaunch& L) {
   using CH = FwdCfg<C::D, C::kBF16, C::kQTiles, C::kStages, 2>;
-  static bool attr_done[64][6] = {};
+  static bool attr_done[64][10] = {};
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -45,11 +45,17 @@ cudaError_t launch_cfg(FwdLaunch& L) {
     L.params.num_units = L.params.units_per_head * L.params.BH;
   }
   bool* done = attr_done[dev];
-  if (L.mod && L.params.cap_in > 0.f)
-    return L.causal ? launch_one<CH, true, true>(L, done[5]) : launch_one<CH, false, true>(L, done[4]);
+  // kWin: spans and masks of a sliding window; kMod: softcap or ALiBi scores
+  if (L.mod && L.params.cap_in > 0.f) {
+    if (L.win)
+      return L.causal ? launch_one<CH, true, true, true>(L, done[9]) : launch_one<CH, false, true, true>(L, done[8]);
+    return L.causal ? launch_one<CH, true, true, false>(L, done[7]) : launch_one<CH, false, true, false>(L, done[6]);
+  }
+  if (L.win)
+    return L.causal ? launch_one<C, true, true, true>(L, done[5]) : launch_one<C, false, true, true>(L, done[4]);
   if (L.mod)
-    return L.causal ? launch_one<C, true, true>(L, done[3]) : launch_one<C, false, true>(L, done[2]);
-  return L.causal ? launch_one<C, true, false>(L, done[1]) : launch_one<C, false, false>(L, done[0]);
+    return L.causal ? launch_one<C, true, true, false>(L, done[3]) : launch_one<C, false, true, false>(L, done[2]);
+  return L.causal ? launch_one<C, true, false, false>(L, done[1]) : launch_one<C, false, false, false>(L, done[0]);
 }
 
 }  // namespace fa2
