@@ -448,7 +448,13 @@ def run_ours(args, rank, local, world):
         e2e_ins = [(q, tq), (k, tk), (v, tv), (o_host, o), (lse.cpu().numpy(), lse), (do, tdo)]
         e2e_outs = [dq, dk, dv]
     host_step = None
-    if not (bwd or w.modified or w.split_kv):
+    if bwd and args.e2e:
+        def host_step(hin, hout):
+            bf = [t.view(torch.bfloat16) if t.dtype == torch.int16 else t for t in hin + hout]
+            fa2.fa2_bwd_host(*bf[:6], dq_host=bf[6], dk_host=bf[7], dv_host=bf[8], scale=w.scale,
+                             causal=w.causal, chunks=args.e2e_chunks, workspace=ws,
+                             buffers=(tq, tk, tv, o, lse, tdo, dq, dk, dv), stream=stream)
+    elif not (bwd or w.modified or w.split_kv):
         def host_step(hin, hout):
             as_dt = (lambda t: t.view(torch.bfloat16)) if w.dtype == si.BF16 else (lambda t: t)
             fa2.fa2_fwd_host(as_dt(hin[0]), as_dt(hin[1]), as_dt(hin[2]), o_host=as_dt(hout[0]),
@@ -456,7 +462,8 @@ def run_ours(args, rank, local, world):
                              causal=w.causal, chunks=args.e2e_chunks, stream=stream)
     e2e = measure_e2e(args, flops, step, stream, world, e2e_ins, e2e_outs, host_step) if args.e2e else None
     if e2e is not None:
-        e2e["api"] = "fa2_fwd_host (pipelined copies)" if host_step else "copies + device-buffer call"
+        e2e["api"] = (("fa2_bwd_host" if bwd else "fa2_fwd_host") + " (pipelined copies)") if host_step \
+            else "copies + device-buffer call"
 
     if rank != 0:
         return

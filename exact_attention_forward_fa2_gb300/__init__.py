@@ -47,6 +47,7 @@ SIGNATURES = {
     "fa2_bwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ,
                  _VP], _I),
     "fa2_bwd_workspace_bytes": ([_I, _I, _I], _SZ),
+    "fa2_bwd_host": ([_VP] * 18 + [_I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _I, _VP], _I),
     "fa2_fwd_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I,
                       _I, _VP], _I),
     "fa2_splitkv_num_splits": ([_I, _I, _I, _I, _I, _I, _I], _I),
@@ -387,6 +388,70 @@ def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale: float | Non
     if rc != FA2_OK:
         raise Fa2Error(rc, "fa2_bwd")
     return dq, dk, dv
+
+
+def fa2_bwd_host(q_host, k_host, v_host, o_host, lse_host, dout_host, dq_host=None, dk_host=None,
+                 dv_host=None, scale: float | None = None, causal: bool = False, chunks: int = 0,
+                 device=None, workspace=None, buffers=None, stream=None):
+    """Backward for host tensors (C ABI ``fa2_bwd_host``): copies q, k, v, o, lse
+    and dout in, computes and copies dq, dk, dv out in slices of heads that overlap
+    one another.  Host tensors (page-locked for overlap) of the ``fa2_bwd`` shapes;
+    the device buffers (``buffers``: q, k, v, o, lse, dout, dq, dk, dv) and the
+    workspace are allocated on ``device`` (default: the current CUDA device) when
+    not given.  Returns (dq_host, dk_host, dv_host); they are valid once ``stream``
+    is synchronised."""
+    import torch
+
+    host_in = (q_host, k_host, v_host, o_host, lse_host, dout_host)
+    if any(t.is_cuda for t in host_in):
+        raise ValueError("inputs must be host tensors")
+    if q_host.dtype != torch.bfloat16 or any(t.dtype != torch.bfloat16 for t in (k_host, v_host, o_host, dout_host)):
+        raise TypeError("q, k, v, o, dout must be bf16")
+    if q_host.dim() != 4 or k_host.dim() != 4 or v_host.shape != k_host.shape \
+            or q_host.shape[0] != k_host.shape[0] or q_host.shape[3] != k_host.shape[3] \
+            or q_host.shape[1] % k_host.shape[1] != 0:
+        raise ValueError("expected q [B,H,M,D] and k, v [B,H_kv,N,D] with H_kv dividing H")
+    B, H, M, D = q_host.shape
+    H_kv, N = k_host.shape[1], k_host.shape[2]
+    if o_host.shape != q_host.shape or dout_host.shape != q_host.shape:
+        raise ValueError("o and dout must be like q")
+    if lse_host.shape != (B, H, M) or lse_host.dtype != torch.float32:
+        raise ValueError("lse must be fp32 [B,H,M]")
+    for t in host_in:
+        if not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous")
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    dq_host = torch.empty(q_host.shape, dtype=torch.bfloat16).pin_memory() if dq_host is None else dq_host
+    dk_host = torch.empty(k_host.shape, dtype=torch.bfloat16).pin_memory() if dk_host is None else dk_host
+    dv_host = torch.empty(k_host.shape, dtype=torch.bfloat16).pin_memory() if dv_host is None else dv_host
+    for t, like in ((dq_host, q_host), (dk_host, k_host), (dv_host, k_host)):
+        if t.shape != like.shape or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.is_cuda:
+            raise ValueError("dq_host must be like q_host, dk_host and dv_host like k_host")
+    if buffers is None:
+        dbuf = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in host_in]
+        dq, dk, dv = (torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for t in (q_host, k_host, k_host))
+    else:
+        if len(buffers) != 9:
+            raise ValueError("buffers: q, k, v, o, lse, dout, dq, dk, dv")
+        dbuf, (dq, dk, dv) = list(buffers[:6]), buffers[6:]
+        for t, like in zip(list(buffers), list(host_in) + [q_host, k_host, k_host]):
+            if not t.is_cuda or t.shape != like.shape or t.dtype != like.dtype or not t.is_contiguous():
+                raise ValueError("device buffers must be contiguous CUDA tensors like the host ones")
+        dev = dbuf[0].device
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(dev):
+        need = lib().fa2_bwd_workspace_bytes(B, H, M)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        rc = lib().fa2_bwd_host(*(t.data_ptr() for t in host_in), dq_host.data_ptr(), dk_host.data_ptr(),
+                                dv_host.data_ptr(), *(t.data_ptr() for t in dbuf), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, H_kv, M, N, D, float(scale), 1 if causal else 0, FA2_BF16,
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(), int(chunks),
+                                _stream_handle(dbuf[0], stream))
+    if rc != FA2_OK:
+        raise Fa2Error(rc, "fa2_bwd_host")
+    return dq_host, dk_host, dv_host
 
 
 # The grouped-query entry has the same Python signature: k and v carry H_kv heads.

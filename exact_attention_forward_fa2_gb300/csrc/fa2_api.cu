@@ -512,6 +512,86 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
   return fa2::launch_bwd(L, D) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
+extern "C" int fa2_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
+                            const float* lse_host, const void* dout_host, void* dq_host, void* dk_host,
+                            void* dv_host, void* q, void* k, void* v, void* o, float* lse, void* dout, void* dq,
+                            void* dk, void* dv, int B, int H, int H_kv, int M, int N, int D, float scale,
+                            int causal, int dtype, void* workspace, size_t workspace_size, int chunks,
+                            void* stream) {
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host || !dout_host || !dq_host || !dk_host || !dv_host)
+    return FA2_ERR_NULL;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA2_ERR_NULL;
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
+  if (D != 64 && D != 128) return FA2_ERR_HEADDIM;
+  if (dtype != FA2_BF16) return FA2_ERR_DTYPE;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA2_ERR_SCALE;
+  const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
+  if ((addr(q) | addr(k) | addr(v) | addr(o) | addr(dout) | addr(dq) | addr(dk) | addr(dv)) & 15u)
+    return FA2_ERR_ALIGN;
+  if (addr(lse) & 3u) return FA2_ERR_ALIGN;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh > INT_MAX) return FA2_ERR_TOO_LARGE;
+  // the whole problem's workspace serves every slice (a slice has fewer heads)
+  if (!workspace || (addr(workspace) & 255u) || workspace_size < bwd_workspace_bytes(bh, M))
+    return FA2_ERR_WORKSPACE;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != FA2_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
+
+  // slices of whole key/value heads with the query heads that read them, as in
+  // fa2_fwd_host: copies in on one library stream, the backward on the caller's
+  // stream, copies out on the other library stream
+  const int group = H / H_kv;
+  const int64_t kv_heads = static_cast<int64_t>(B) * H_kv;
+  if (chunks <= 0) chunks = 4;
+  chunks = static_cast<int>(std::min<int64_t>({static_cast<int64_t>(chunks), kv_heads, kHostMaxChunks}));
+  const size_t q_head = static_cast<size_t>(M) * D * 2, kv_head = static_cast<size_t>(N) * D * 2;
+  const size_t l_head = static_cast<size_t>(M) * sizeof(float);
+  const cudaStream_t s0 = static_cast<cudaStream_t>(stream);
+  auto at = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+  auto atw = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+
+  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(dev, &hp);
+  if (rc != FA2_OK) return rc;
+  bool ok = cudaEventRecord(hp->start, s0) == cudaSuccess && cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess;
+  for (int c = 0; ok && c < chunks; ++c) {
+    const int64_t g0 = kv_heads * c / chunks, g1 = kv_heads * (c + 1) / chunks;
+    const int64_t nq = (g1 - g0) * group, q0 = g0 * group;
+    const size_t qo = q0 * q_head, ko = g0 * kv_head;
+    ok = cudaMemcpyAsync(atw(q, qo), at(q_host, qo), nq * q_head, cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(atw(k, ko), at(k_host, ko), (g1 - g0) * kv_head, cudaMemcpyHostToDevice, hp->h2d) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(atw(v, ko), at(v_host, ko), (g1 - g0) * kv_head, cudaMemcpyHostToDevice, hp->h2d) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(atw(o, qo), at(o_host, qo), nq * q_head, cudaMemcpyHostToDevice, hp->h2d) == cudaSuccess &&
+         cudaMemcpyAsync(lse + q0 * M, lse_host + q0 * M, nq * l_head, cudaMemcpyHostToDevice, hp->h2d) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(atw(dout, qo), at(dout_host, qo), nq * q_head, cudaMemcpyHostToDevice, hp->h2d) ==
+             cudaSuccess &&
+         cudaEventRecord(hp->in[c], hp->h2d) == cudaSuccess && cudaStreamWaitEvent(s0, hp->in[c], 0) == cudaSuccess;
+    if (!ok) break;
+    // these heads as a problem of their own: batch 1, nq query heads, g1 - g0 key/value heads
+    rc = fa2_bwd(at(q, qo), at(k, ko), at(v, ko), at(o, qo), lse + q0 * M, at(dout, qo), atw(dq, qo), atw(dk, ko),
+                 atw(dv, ko), 1, static_cast<int>(nq), static_cast<int>(g1 - g0), M, N, D, scale, causal, dtype,
+                 workspace, workspace_size, s0);
+    if (rc != FA2_OK) return rc;
+    ok = cudaEventRecord(hp->done[c], s0) == cudaSuccess && cudaStreamWaitEvent(hp->d2h, hp->done[c], 0) == cudaSuccess &&
+         cudaMemcpyAsync(atw(dq_host, qo), at(dq, qo), nq * q_head, cudaMemcpyDeviceToHost, hp->d2h) == cudaSuccess &&
+         cudaMemcpyAsync(atw(dk_host, ko), at(dk, ko), (g1 - g0) * kv_head, cudaMemcpyDeviceToHost, hp->d2h) ==
+             cudaSuccess &&
+         cudaMemcpyAsync(atw(dv_host, ko), at(dv, ko), (g1 - g0) * kv_head, cudaMemcpyDeviceToHost, hp->d2h) ==
+             cudaSuccess;
+  }
+  // the caller's stream reaches its next work only after the last copy back
+  ok = ok && cudaEventRecord(hp->out_done, hp->d2h) == cudaSuccess &&
+       cudaStreamWaitEvent(s0, hp->out_done, 0) == cudaSuccess;
+  return ok ? FA2_OK : FA2_ERR_CUDA;
+}
+
 extern "C" const char* fa2_strerror(int status) {
   switch (status) {
     case FA2_OK: return "ok";

@@ -240,6 +240,30 @@ int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, voi
                  int H_kv, int M, int N, int D, float scale, int causal, int dtype, int chunks,
                  void* stream);
 
+/*
+ * fa2_bwd_host -- the backward for inputs and outputs in HOST memory, pipelined
+ * like fa2_fwd_host: slice by slice of whole key/value heads (with the query
+ * heads that read them), q, k, v, o, lse and dout are copied in on a library
+ * stream, fa2_bwd runs on `stream`, and dq, dk, dv are copied back on a second
+ * library stream, so one slice's copies overlap the other slices' kernels.
+ * `stream` reaches its next work only after the last copy back.
+ *
+ *   *_host          host buffers of the fa2_bwd shapes: q, k, v, o, lse, dout are
+ *                   only read; dq, dk, dv are overwritten
+ *   q ... dv        DEVICE buffers of the same shapes (caller-owned); q, k, v, o,
+ *                   lse, dout are overwritten by the copies
+ *   workspace       as fa2_bwd, sized for the whole problem (every slice reuses it)
+ *   chunks          slices (<= 0: 4); at most B*H_kv and 32
+ * Host buffers should be page-locked.  Other arguments and errors as fa2_bwd and
+ * fa2_fwd_host; the result equals fa2_bwd's bitwise (each slice is its own
+ * problem with the same kernels).  The pages have no counterpart to this entry.
+ */
+int fa2_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
+                 const float* lse_host, const void* dout_host, void* dq_host, void* dk_host, void* dv_host,
+                 void* q, void* k, void* v, void* o, float* lse, void* dout, void* dq, void* dk, void* dv,
+                 int B, int H, int H_kv, int M, int N, int D, float scale, int causal, int dtype,
+                 void* workspace, size_t workspace_size, int chunks, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* fa2_strerror(int status);
 

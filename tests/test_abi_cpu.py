@@ -31,7 +31,7 @@ def lib():
 
 
 def test_header_declares_the_api():
-    assert declared_functions() == ["fa2_bwd", "fa2_bwd_workspace_bytes", "fa2_device_status", "fa2_fwd",
+    assert declared_functions() == ["fa2_bwd", "fa2_bwd_host", "fa2_bwd_workspace_bytes", "fa2_device_status", "fa2_fwd",
                                     "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_host", "fa2_fwd_splitkv",
                                     "fa2_fwd_splitkv_noalloc", "fa2_selftest_wait_timeout",
                                     "fa2_splitkv_num_splits", "fa2_splitkv_workspace_bytes", "fa2_strerror",
@@ -198,6 +198,25 @@ def call_host(lib, **kw):
 ])
 def test_host_entry_rejects_bad_arguments(lib, kw, code):
     assert call_host(lib, **kw) == code
+
+
+def call_bwd_host(lib, **kw):
+    a = dict(h=P, q=P, B=2, H=4, H_kv=2, M=64, N=64, D=64, scale=0.125, causal=0, dtype=0, ws=P, ws_bytes=1 << 20,
+             chunks=0, lh=P, dqh=P)
+    a.update(kw)
+    return lib.fa2_bwd_host(a["h"], a["h"], a["h"], a["h"], a["lh"], a["h"], a["dqh"], a["h"], a["h"],
+                            a["q"], P, P, P, P, P, P, P, P, a["B"], a["H"], a["H_kv"], a["M"], a["N"], a["D"],
+                            a["scale"], a["causal"], a["dtype"], a["ws"], a["ws_bytes"], a["chunks"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=None), fa2.FA2_ERR_NULL), (dict(lh=None), fa2.FA2_ERR_NULL), (dict(dqh=None), fa2.FA2_ERR_NULL),
+    (dict(q=None), fa2.FA2_ERR_NULL), (dict(H_kv=3), fa2.FA2_ERR_SHAPE), (dict(D=32), fa2.FA2_ERR_HEADDIM),
+    (dict(dtype=1), fa2.FA2_ERR_DTYPE), (dict(scale=-1.0), fa2.FA2_ERR_SCALE), (dict(q=P + 4), fa2.FA2_ERR_ALIGN),
+    (dict(ws=None), fa2.FA2_ERR_WORKSPACE), (dict(ws_bytes=1024), fa2.FA2_ERR_WORKSPACE),
+])
+def test_bwd_host_entry_rejects_bad_arguments(lib, kw, code):
+    assert call_bwd_host(lib, **kw) == code
 
 
 @pytest.mark.parametrize("limit", [0, -5, 2001])

@@ -1,8 +1,8 @@
-"""The host-buffer entry fa2_fwd_host: copies in slices of heads overlapped
-with the compute of other slices.  Each slice is computed by the same kernel as
-a whole-problem call, so the outputs must equal fa2_fwd's bitwise, for any
-number of slices, grouped-query heads and page-locked or pageable host memory;
-one case is also checked against the oracle."""
+"""The host-buffer entries fa2_fwd_host and fa2_bwd_host: copies in slices of
+heads overlapped with the compute of other slices.  Each slice is computed by the
+same kernels as a whole-problem call, so the outputs must equal fa2_fwd's (and
+fa2_bwd's) bitwise, for any number of slices, grouped-query heads and page-locked
+or pageable host memory; one forward case is also checked against the oracle."""
 import numpy as np
 import pytest
 
@@ -90,3 +90,32 @@ def test_host_entry_back_to_back_calls(fa2):
         o_d, l_d = fa2.fa2_fwd(host(q).cuda(), host(k).cuda(), host(v).cuda())
         torch.cuda.synchronize()
         assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
+BWD_CASES = [  # (B, H, H_kv, M, N, D, causal)
+    (2, 4, 4, 300, 500, 128, True),
+    (1, 8, 2, 257, 257, 64, False),
+    (2, 6, 3, 130, 700, 128, True),
+    (1, 1, 1, 1, 1, 64, False),
+]
+
+
+@pytest.mark.parametrize("chunks", [0, 1, 3, 99])
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_host_backward_equals_device_backward(fa2, case, chunks):
+    """fa2_bwd_host: the same kernels per slice of heads, so dq, dk, dv equal
+    fa2_bwd's bitwise for any number of slices."""
+    B, H, Hkv, M, N, D, causal = case
+    q = si.normal(510, 1, (B, H, M, D), 1.0, si.BF16)
+    k = si.normal(510, 2, (B, Hkv, N, D), 1.0, si.BF16)
+    v = si.normal(510, 3, (B, Hkv, N, D), 1.0, si.BF16)
+    do = si.normal(510, 4, (B, H, M, D), 1.0, si.BF16)
+    hq, hk, hv, hdo = host(q), host(k), host(v), host(do)
+    o, lse = fa2.fa2_fwd(hq.cuda(), hk.cuda(), hv.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    ho, hl = o.cpu().pin_memory(), lse.cpu().pin_memory()
+    dq_h, dk_h, dv_h = fa2.fa2_bwd_host(hq, hk, hv, ho, hl, hdo, causal=causal, chunks=chunks)
+    torch.cuda.synchronize()
+    dq, dk, dv = fa2.fa2_bwd(hq.cuda(), hk.cuda(), hv.cuda(), o, lse, hdo.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(dq_h, dq.cpu()) and torch.equal(dk_h, dk.cpu()) and torch.equal(dv_h, dv.cpu())
