@@ -59,6 +59,16 @@ def measured_peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def peak_sustained():
+    """The bf16 sustained peak (seconds-long cuBLAS loop) from MEASURED_PEAKS.json,
+    or None."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f).get("bf16_tflops_sustained")
+    return None
+
+
 # Sources each timed pass is built from: a profile summary stays valid while these are unchanged.
 PASS_SOURCES = {
     "fwd": ("fa2_fwd_kernel.cuh", "fa2_launch.cuh", "fa2_config.h", "sm103_ptx.cuh",
@@ -358,6 +368,68 @@ def measure_e2e(args, flops, step, stream, world, ins, outs, host_step=None):
 
 
 # ------------------------------------------------------------------ GPU path
+def measure_sustained(seconds, flops, step, stream, local, launch_s):
+    """Back-to-back launches for about ``seconds`` on the launching stream, with
+    no L2 flush between them: the rate a long run settles at under the power cap
+    (timed with one CUDA event pair around the whole run)."""
+    import torch
+    n = max(3, min(200000, int(seconds / max(launch_s, 1e-6))))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    dt = e0.elapsed_time(e1) / 1e3
+    return {"value": flops * n / dt / 1e12, "unit": UNIT, "seconds": dt, "launches": n,
+            "l2": "not flushed (back-to-back launches)", "clocks": clocks.summary()}
+
+
+def tf32_matmul_peak(dev, n: int = 8192, reps: int = 10) -> float:
+    """Dense TF32 tensor throughput of this GPU, measured here: the best of
+    ``reps`` cuBLAS fp32 matmuls of n^3 with TF32 allowed (2 n^3 FLOP each)."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        best = float("inf")
+        for i in range(reps + 3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            e1.synchronize()
+            if i >= 3:
+                best = min(best, e0.elapsed_time(e1) / 1e3)
+        del a, b, c
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / best / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def sfu_probe(fa2, local, flops_per_exp: float, peak_tflops: float):
+    """The special-function pipe's ex2 rate (the library's probe kernel) against
+    the exponentials the softmax needs at the tensor peak: one per score element,
+    i.e. peak / (4 D) per second in the forward."""
+    import torch
+    with ClockSampler(local) as clocks:
+        rate = fa2.fa2_probe_ex2()
+    summ = clocks.summary()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    out = {"ex2_per_s": rate, "demand_at_peak_per_s": peak_tflops * 1e12 / flops_per_exp}
+    out["demand_frac"] = out["demand_at_peak_per_s"] / rate
+    if summ and summ["sm_mhz"] > 0:
+        out["ex2_per_clk_per_sm"] = rate / (sms * summ["sm_mhz"] * 1e6)
+        out["sm_mhz"] = summ["sm_mhz"]
+    return out
+
+
 def run_ours(args, rank, local, world):
     import torch
     import exact_attention_forward_fa2_gb300 as fa2
@@ -465,15 +537,32 @@ def run_ours(args, rank, local, world):
         e2e["api"] = (("fa2_bwd_host" if bwd else "fa2_fwd_host") + " (pipelined copies)") if host_step \
             else "copies + device-buffer call"
 
+    launch_s = sum(kernel_ms) / len(kernel_ms) / 1e3
+    sustained = None
+    if args.sustained_s > 0 and launch_s < 100e-6:
+        sustained = {"skipped": "launches shorter than 100 us: a back-to-back loop issued from Python "
+                                "would measure the host, not the GPU"}
+    elif args.sustained_s > 0:
+        sustained = measure_sustained(args.sustained_s, flops, step, stream, local, launch_s)
+    if fa2.fa2_device_status(reset=True) != 0:
+        raise RuntimeError("device status set during the sustained run")
+
     if rank != 0:
         return
     peak, hbm_peak, peak_kind = measured_peaks()
     peak_kind = f"bf16 dense burst, {peak_kind}"
+    tf32_probe = None
     if w.dtype != si.BF16:
-        # TF32 contraction: the measured bf16 peak times the nominal dense TF32/BF16 ratio
-        peak = peak * TF32_OVER_BF16
-        peak_kind = f"tf32 = {TF32_OVER_BF16:.3f} x {peak_kind} (nominal 1.1/2.25 PFLOP/s)"
-    launch_s = sum(kernel_ms) / len(kernel_ms) / 1e3
+        # TF32 contraction: this GPU's TF32 rate, measured by a cuBLAS matmul probe
+        tf32_probe = tf32_matmul_peak(dev)
+        peak = tf32_probe
+        peak_kind = ("tf32 dense burst, measured in this run (cuBLAS fp32 8192^3 matmul with TF32, "
+                     f"best of 10); nominal ratio would give {TF32_OVER_BF16 * measured_peaks()[0]:.1f}")
+    sus_peak = peak_sustained() if w.dtype == si.BF16 else None
+    if sustained is not None and "value" in sustained and sus_peak:
+        sustained["peak"] = sus_peak
+        sustained["frac"] = sustained["value"] / sus_peak
+        sustained["peak_kind"] = "bf16 dense sustained (4 s back-to-back cuBLAS), measured"
     achieved = flops / launch_s / 1e12
     io = w.io_bytes()
     # below the ridge (peak FLOP/s over peak HBM bytes/s) the launch is bound by
@@ -508,6 +597,8 @@ def run_ours(args, rank, local, world):
                      "hbm_gbs_at_this_time": w.io_bytes() / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e9,
                      "hbm_peak_gbs": hbm_peak},
         "e2e": e2e,
+        "sustained": sustained,
+        "sfu": None if bwd or w.dtype != si.BF16 else sfu_probe(fa2, local, 4.0 * w.D, peak),
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "device_status": status,
@@ -539,6 +630,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--sustained-s", type=float, default=4.0,
+                    help="seconds of back-to-back launches after the timed steps (0: skip)")
     ap.add_argument("--e2e-chunks", type=int, default=0,
                     help="head slices of the host-buffer pipeline (0: the library's choice)")
     ap.add_argument("--clock-log", default=None, help="write the NVML clock samples here (CSV)")

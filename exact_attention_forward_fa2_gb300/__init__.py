@@ -55,6 +55,7 @@ SIGNATURES = {
     "fa2_selftest_wait_timeout": ([_I, _VP], _I),
     "fa2_strerror": ([_I], ctypes.c_char_p),
     "fa2_device_status": ([_I, ctypes.POINTER(_I)], _I),
+    "fa2_probe_ex2": ([_VP, _I, _I, _VP], _I),
     "fa2_version": ([], _I),
 }
 
@@ -112,6 +113,33 @@ def fa2_selftest_wait_timeout(limit_ms: int = 20, stream=None) -> None:
     rc = lib().fa2_selftest_wait_timeout(int(limit_ms), handle)
     if rc != FA2_OK:
         raise Fa2Error(rc, "fa2_selftest_wait_timeout")
+
+
+def fa2_probe_ex2(blocks: int | None = None, iters: int = 4096, reps: int = 5, stream=None) -> float:
+    """Exponentials per second of the special-function pipe's ex2 on the current
+    device (C ABI ``fa2_probe_ex2``): the median over ``reps`` launches of
+    ``blocks`` CTAs (default 8 per SM, full occupancy), each timed with CUDA
+    events on ``stream``.  A measurement aid for the softmax's ceiling."""
+    import torch
+    dev = torch.cuda.current_device()
+    if blocks is None:
+        blocks = 8 * torch.cuda.get_device_properties(dev).multi_processor_count
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    handle = _stream_handle(out, stream)
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    times = []
+    for i in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        rc = lib().fa2_probe_ex2(out.data_ptr(), int(blocks), int(iters), handle)
+        if rc != FA2_OK:
+            raise Fa2Error(rc, "fa2_probe_ex2")
+        e1.record(s)
+        e1.synchronize()
+        if i > 0:  # the first launch is a warm-up
+            times.append(e0.elapsed_time(e1) / 1e3)
+    times.sort()
+    return blocks * 256 * 8 * iters / times[len(times) // 2]
 
 
 def _check_qkv(q, k, v):

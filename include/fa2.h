@@ -291,6 +291,21 @@ int fa2_device_status(int reset, int* raw_code);
  */
 int fa2_selftest_wait_timeout(int limit_ms, void* stream);
 
+/*
+ * fa2_probe_ex2 -- throughput probe of the base-2 exponential of the special-
+ * function pipe (the ex2 the softmax of both passes is built on; the pages'
+ * "Writing FlashAttention 2 in Triton", Step 5, swaps exp for exp2 for this
+ * reason).  Launches `blocks` CTAs of 256 threads on `stream`; every thread runs
+ * 8 independent chains of `iters` steps, each step one ex2 and one add, and
+ * writes one float to out[blocks * 256] (device, caller-owned, 4-byte aligned).
+ * The caller times the launch: exponentials = blocks * 256 * 8 * iters.  A
+ * measurement aid only; no result of the attention path depends on it.
+ * Returns FA2_OK when launched, FA2_ERR_NULL, FA2_ERR_SHAPE (blocks outside
+ * 1..65536 or iters outside 1..2^20), FA2_ERR_ALIGN, FA2_ERR_ARCH or
+ * FA2_ERR_CUDA.
+ */
+int fa2_probe_ex2(float* out, int blocks, int iters, void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int fa2_version(void);
 

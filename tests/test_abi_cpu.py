@@ -33,7 +33,7 @@ def lib():
 def test_header_declares_the_api():
     assert declared_functions() == ["fa2_bwd", "fa2_bwd_host", "fa2_bwd_workspace_bytes", "fa2_device_status", "fa2_fwd",
                                     "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_host", "fa2_fwd_splitkv",
-                                    "fa2_fwd_splitkv_noalloc", "fa2_selftest_wait_timeout",
+                                    "fa2_fwd_splitkv_noalloc", "fa2_probe_ex2", "fa2_selftest_wait_timeout",
                                     "fa2_splitkv_num_splits", "fa2_splitkv_workspace_bytes", "fa2_strerror",
                                     "fa2_version"]
 
@@ -222,6 +222,19 @@ def test_bwd_host_entry_rejects_bad_arguments(lib, kw, code):
 @pytest.mark.parametrize("limit", [0, -5, 2001])
 def test_selftest_rejects_limits_out_of_range(lib, limit):
     assert lib.fa2_selftest_wait_timeout(limit, None) == fa2.FA2_ERR_SHAPE
+
+
+@pytest.mark.parametrize("out,blocks,iters,code", [
+    (None, 8, 16, fa2.FA2_ERR_NULL),
+    (256, 0, 16, fa2.FA2_ERR_SHAPE),
+    (256, 65537, 16, fa2.FA2_ERR_SHAPE),
+    (256, 8, 0, fa2.FA2_ERR_SHAPE),
+    (256, 8, (1 << 20) + 1, fa2.FA2_ERR_SHAPE),
+    (258, 8, 16, fa2.FA2_ERR_ALIGN),
+])
+def test_ex2_probe_rejects_bad_arguments(lib, out, blocks, iters, code):
+    # checked before any CUDA call, so no device is needed
+    assert lib.fa2_probe_ex2(out, blocks, iters, None) == code
 
 
 def test_no_gpu_means_an_error_not_a_fallback(lib):
