@@ -15,10 +15,10 @@ the oracle gets the exact bf16 values of the rows it checks, copied back.
   backward of the sub-problem made of the sampled rows gives the exact dK and
   dV of the whole problem, and its dQ on those rows: all three are checked
   against the oracle's attn_bwd on that sub-problem, while the kernels still
-  stream all 8.4M query rows.  (A dO that is nonzero everywhere would make dK
-  and dV sums of 8.4M terms, whose fp32 accumulation on the tensor core drifts
-  by ~1% of their size: a property of the accumulation length, not of the
-  indexing under test.)  Bar: max |GPU - oracle| <= 1e-2 max |oracle| + 1e-5,
+  stream all 8.4M query rows.  (With a dO that is nonzero everywhere, dK and dV
+  are sums of 8.4M terms and came out ~1% of their size from a chunked fp32
+  reference: an effect of the accumulation length, which is not what this test
+  is about.)  Bar: max |GPU - oracle| <= 1e-2 max |oracle| + 1e-5,
   as in the backward parity tests; rows without dO must get dQ = 0 exactly.
 """
 import math
