@@ -255,7 +255,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
-// Backward workspace: L log2(e) and D = rowsum(dO o O), [B*H][M rounded up to 128] fp32 each.
+// Backward workspace: -L log2(e) and D = rowsum(dO o O), [B*H][M rounded up to 128] fp32 each.
 size_t bwd_workspace_bytes(int64_t bh, int M) {
   const int64_t mpad = (static_cast<int64_t>(M) + 127) / 128 * 128;
   return 2 * static_cast<size_t>(bh * mpad) * sizeof(float);
@@ -488,9 +488,9 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
   if (rc == FA2_OK) rc = encode_map(&L.tmdQ, dq, dtype, D, M, bh);
   if (rc != FA2_OK) return rc;
   const int64_t mpad = n_qtiles * 128;
-  L.lse2 = static_cast<float*>(workspace);
-  L.dlt = L.lse2 + bh * mpad;
-  L.params.lse2 = L.lse2;
+  L.nl2 = static_cast<float*>(workspace);
+  L.dlt = L.nl2 + bh * mpad;
+  L.params.nl2 = L.nl2;
   L.params.dlt = L.dlt;
   L.params.status = st->status;
   L.params.M = M;

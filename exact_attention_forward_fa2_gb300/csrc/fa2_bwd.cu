@@ -44,7 +44,7 @@ cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
   const int64_t need = (rows_pad + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
   bwd_preprocess_kernel<D><<<blocks, 256, 0, L.stream>>>(
-      static_cast<const __nv_bfloat16*>(L.o), static_cast<const __nv_bfloat16*>(L.dout), L.lse, L.lse2, L.dlt,
+      static_cast<const __nv_bfloat16*>(L.o), static_cast<const __nv_bfloat16*>(L.dout), L.lse, L.nl2, L.dlt,
       L.params.M, L.params.Mpad, rows_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -11,8 +11,8 @@
 // The N x N matrices P and dS exist only tile by tile, in TMEM.
 //
 // Three launches:
-//   bwd_preprocess    D_i and L_i log2(e) per query row into a padded workspace
-//                     (rows past M get D = 0 and L = +inf, so their P is 0)
+//   bwd_preprocess    D_i and -L_i log2(e) per query row into a padded workspace
+//                     (rows past M get D = 0 and -L log2(e) = -inf, so their P is 0)
 //   bwd_dkdv_kernel   one CTA per (batch, key/value head, 128-key tile): the pages'
 //                     K/V-outer loop.  It streams 64-row tiles of Q and dO (over
 //                     every query head of the group) and accumulates dV and dK
@@ -40,7 +40,7 @@
 namespace fa2 {
 
 struct BwdParams {
-  const float* lse2;  // [BH][Mpad]: L * log2(e); rows >= M: +inf
+  const float* nl2;   // [BH][Mpad]: -L * log2(e); rows >= M: -inf
   const float* dlt;   // [BH][Mpad]: rowsum(dO o O); rows >= M: 0
   int* status;        // sticky device status word
   int M, N, Mpad;     // Mpad = M rounded up to 128
@@ -62,12 +62,13 @@ enum : int {
 
 // ------------------------------------------------------------------ preprocess
 // One warp per query row: D_i = sum_d dO[i,d] O[i,d] in fp32 from bf16, and
-// L_i log2(e).  Rows in [M, Mpad) of every head get D = 0, L = +inf.
+// -L_i log2(e), the exponent offset of P = exp2(s scale log2(e) - L_i log2(e)).
+// Rows in [M, Mpad) of every head get D = 0 and -inf.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
-                                                             float* __restrict__ lse2,
+                                                             float* __restrict__ nl2,
                                                              float* __restrict__ dlt, int M, int Mpad,
                                                              int64_t rows_pad) {
   constexpr int kPer = D / 32;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
     for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
     if (lane == 0) {
       dlt[r] = acc;
-      lse2[r] = i < M ? lse[bh * M + i] * 1.4426950408889634f : INFINITY;
+      nl2[r] = i < M ? lse[bh * M + i] * -1.4426950408889634f : -INFINITY;
     }
   }
 }
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tma_load_3d_hint(base + Lay::do_off(s) + cb * C::kStrBlock, &tmdO, fb, cb * 64, row0, bh, pol_str);
         }
         const int64_t vec = static_cast<int64_t>(bh) * p.Mpad + row0;
-        bulk_load_1d(base + Lay::l2_off(s), p.lse2 + vec, C::BS * 4, fb);
+        bulk_load_1d(base + Lay::l2_off(s), p.nl2 + vec, C::BS * 4, fb);
         bulk_load_1d(base + Lay::dl_off(s), p.dlt + vec, C::BS * 4, fb);
         issued = t + 1;
       }
@@ -367,27 +368,54 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
       reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
       const int row0 = step_row0(t);
-      // causal: query row0 + c sees this key iff row0 + c >= key (diagonal steps only)
-      const int lim = (kCausal && row0 < key0 + C::BF) ? key - row0 : -1;
       uint32_t pk[32], dk[32];
+      if ((!kCausal || row0 >= key0 + C::BF) && key0 + C::BF <= p.N) {
+        // every query of the step sees every key of the tile: no mask, and the
+        // arithmetic on packed pairs (one FFMA2, FSUB2 and FMUL2 per two scores)
+        const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
 #pragma unroll
-      for (int c4 = 0; c4 < C::BS; c4 += 4) {
-        float l2[4], dl[4];
-        ld_shared_v4(base + Lay::l2_off(s) + c4 * 4, l2[0], l2[1], l2[2], l2[3]);
-        ld_shared_v4(base + Lay::dl_off(s) + c4 * 4, dl[0], dl[1], dl[2], dl[3]);
-        float pv[4], dsv[4];
+        for (int c4 = 0; c4 < C::BS; c4 += 4) {
+          float l2[4], dl[4];
+          ld_shared_v4(base + Lay::l2_off(s) + c4 * 4, l2[0], l2[1], l2[2], l2[3]);
+          ld_shared_v4(base + Lay::dl_off(s) + c4 * 4, dl[0], dl[1], dl[2], dl[3]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = c4 + e;
-          const bool vis = key_ok && c >= lim;
-          const float pe = vis ? ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -l2[e])) : 0.f;
-          pv[e] = pe;
-          dsv[e] = pe * (__uint_as_float(dv[c]) - dl[e]);
+          for (int e = 0; e < 4; e += 2) {
+            const int c = c4 + e;
+            float x0, x1, d0, d1;
+            unpack_f32x2(ffma2(pack_f32x2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                               pack_f32x2(l2[e], l2[e + 1])),
+                         x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            unpack_f32x2(fmul2(pack_f32x2(p0, p1),
+                               fsub2(pack_f32x2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])),
+                                     pack_f32x2(dl[e], dl[e + 1]))),
+                         d0, d1);
+            pk[c / 2] = pack_bf16x2(p0, p1);
+            dk[c / 2] = pack_bf16x2(d0, d1);
+          }
         }
-        pk[c4 / 2] = pack_bf16x2(pv[0], pv[1]);
-        pk[c4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-        dk[c4 / 2] = pack_bf16x2(dsv[0], dsv[1]);
-        dk[c4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+      } else {
+        // causal: query row0 + c sees this key iff row0 + c >= key (diagonal steps only)
+        const int lim = (kCausal && row0 < key0 + C::BF) ? key - row0 : -1;
+#pragma unroll
+        for (int c4 = 0; c4 < C::BS; c4 += 4) {
+          float l2[4], dl[4];
+          ld_shared_v4(base + Lay::l2_off(s) + c4 * 4, l2[0], l2[1], l2[2], l2[3]);
+          ld_shared_v4(base + Lay::dl_off(s) + c4 * 4, dl[0], dl[1], dl[2], dl[3]);
+          float pv[4], dsv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c4 + e;
+            const bool vis = key_ok && c >= lim;
+            const float pe = vis ? ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, l2[e])) : 0.f;
+            pv[e] = pe;
+            dsv[e] = pe * (__uint_as_float(dv[c]) - dl[e]);
+          }
+          pk[c4 / 2] = pack_bf16x2(pv[0], pv[1]);
+          pk[c4 / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk[c4 / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          dk[c4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+        }
       }
       tmem_st_x32(tmem + lane_addr + C::kColS(ts), pk);
       tmem_st_x32(tmem + lane_addr + C::kColDP(ts), dk);
@@ -694,13 +722,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int row = tile_row0 + r;
     const int n_t = (dq_key_end<kCausal>(tile_row0, p.M, p.N) + C::BS - 1) / C::BS;
     const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    float l2 = INFINITY, dl = 0.f;
+    float l2 = -INFINITY, dl = 0.f;  // -L log2(e) and D of this row
     if (n_t > 0) {
       const int64_t vec = static_cast<int64_t>(bh) * p.Mpad + row;  // row < Mpad when the tile is in range
-      l2 = p.lse2[vec];
+      l2 = p.nl2[vec];
       dl = p.dlt[vec];
     }
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = pack_f32x2(sl2, sl2), l2x2 = pack_f32x2(l2, l2), dlx2 = pack_f32x2(dl, dl);
     bool ok = n_t > 0;
     for (int j = 0; ok && j < n_t; ++j) {
       ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(C::kBarSFull + t), j & 1, kStatusBwdTimeoutSoftmax));
@@ -721,15 +750,30 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       int lim = p.N - 1 - kbase;
       if (kCausal) lim = min(lim, row - kbase);
       uint32_t dk[32];
+      if (__all_sync(0xffffffffu, lim >= C::BS - 1)) {
+        // every key of the step is visible to every row of the warp: no mask, and
+        // the arithmetic on packed pairs
 #pragma unroll
-      for (int c = 0; c < C::BS; c += 2) {
-        float d2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float pe = (c + e <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[c + e]), sl2, -l2)) : 0.f;
-          d2[e] = pe * (__uint_as_float(dv[c + e]) - dl);
+        for (int c = 0; c < C::BS; c += 2) {
+          float x0, x1, d0, d1;
+          unpack_f32x2(ffma2(pack_f32x2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2, l2x2), x0,
+                       x1);
+          unpack_f32x2(fmul2(pack_f32x2(ex2_approx(x0), ex2_approx(x1)),
+                             fsub2(pack_f32x2(__uint_as_float(dv[c]), __uint_as_float(dv[c + 1])), dlx2)),
+                       d0, d1);
+          dk[c / 2] = pack_bf16x2(d0, d1);
         }
-        dk[c / 2] = pack_bf16x2(d2[0], d2[1]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::BS; c += 2) {
+          float d2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float pe = (c + e <= lim) ? ex2_approx(fmaf(__uint_as_float(sv[c + e]), sl2, l2)) : 0.f;
+            d2[e] = pe * (__uint_as_float(dv[c + e]) - dl);
+          }
+          dk[c / 2] = pack_bf16x2(d2[0], d2[1]);
+        }
       }
       tmem_st_x32(tmem + lane_addr + C::kColS(t), dk);
       tmem_st_wait();
@@ -791,7 +835,7 @@ struct BwdLaunch {
   const void* o;
   const void* dout;
   const float* lse;
-  float* lse2;
+  float* nl2;
   float* dlt;
   int causal;
   cudaStream_t stream;
