@@ -99,6 +99,42 @@ def test_sharp_scores_ragged(fa2):
         assert excess <= 0 and el <= TOL[si.BF16], (causal, eo, el)
 
 
+def ramp_inputs(seed, B, H, M, N, D, dtype, sigma, lo, hi):
+    """Keys scaled by a factor rising linearly from lo to hi along the key axis,
+    so every score row's max climbs from tile to tile: by small steps that the
+    kernel leaves in a lagging exponent base (up to 24 in log2 units) and across
+    that bound, where the base moves and O is rescaled."""
+    q = si.normal(seed, 1, (B, H, M, D), sigma, dtype)
+    k = si.normal(seed, 2, (B, H, N, D), sigma, dtype)
+    v = si.normal(seed, 3, (B, H, N, D), 1.0, dtype)
+    r = (lo + (hi - lo) * np.arange(N) / max(N - 1, 1))[:, None]
+    if dtype == si.BF16:
+        k = si.f64_to_bf16_bits(si.bf16_bits_to_f32(k).astype(np.float64) * r)
+    else:
+        k = (k.astype(np.float64) * r).astype(np.float32)
+    return q, k, v
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_rising_row_max(fa2, D):
+    """Row maxima that rise over the key tiles (to ~38 in log2 units): a lagging
+    exponent base, and base moves with O rescales, against the oracle.  bf16 only:
+    the softmax code is the same for both input types, and TF32 products carry a
+    score error that grows with the score (the tensor core keeps 10 mantissa bits
+    of each fp32 operand).  On an fp32 version of these inputs (sigma 1.5, keys
+    scaled up to 2x, D = 64) the fp64 oracle run on Q and K truncated to TF32
+    already differs from the exact L by 0.0148, past the fp32 bound of 5e-3,
+    whatever the kernel does with the exponent base."""
+    dtype = si.BF16
+    B, H, M, N = 1, 2, 300, 1500
+    q, k, v = ramp_inputs(7, B, H, M, N, D, dtype, 2.0, 0.1, 2.5)
+    for causal in (False, True):
+        o, lse = run_gpu(fa2, q, k, v, D ** -0.5, causal)
+        o_ref, l_ref = oracle.attn_fwd(q, k, v, D ** -0.5, causal)
+        eo, el, excess = compare(o, lse, o_ref, l_ref, dtype)
+        assert excess <= 0 and el <= TOL[dtype], (causal, eo, el)
+
+
 def test_other_scales(fa2):
     B, H, M, N, D = 1, 2, 150, 260, 64
     q, k, v = inputs(5, B, H, M, N, D, si.BF16)
