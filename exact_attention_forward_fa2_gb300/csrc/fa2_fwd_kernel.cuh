@@ -248,6 +248,22 @@ __device__ __forceinline__ float tanh_ex2(float x) {
   return copysignf(__fdividef(1.0f - t, 1.0f + t), x);
 }
 
+// tanh of two values with packed fp32x2 arithmetic, from tanh x = (1 - t) / (1 + t)
+// with t = e^(-2x) = 2^(-2 log2(e) x).  The exponent is capped at 64: below
+// x = -22 tanh is -1 to fp32 precision, and t stays finite.  Near 0 the absolute
+// error stays ~1e-7 (1 - t cancels against 1), elsewhere it is relative.
+__device__ __forceinline__ void tanh2_ex2(float& a, float& b) {
+  float u0, u1;
+  ptx::unpack_f32x2(ptx::fmul2(ptx::pack_f32x2(a, b), ptx::pack_f32x2(-2.8853900817779268f, -2.8853900817779268f)),
+                    u0, u1);
+  const uint64_t t2 = ptx::pack_f32x2(ptx::ex2_approx(fminf(u0, 64.f)), ptx::ex2_approx(fminf(u1, 64.f)));
+  const uint64_t one2 = ptx::pack_f32x2(1.f, 1.f);
+  const uint64_t num = ptx::ffma2(t2, ptx::pack_f32x2(-1.f, -1.f), one2);  // 1 - t
+  float d0, d1;
+  ptx::unpack_f32x2(ptx::fadd2(t2, one2), d0, d1);  // 1 + t
+  ptx::unpack_f32x2(ptx::fmul2(num, ptx::pack_f32x2(ptx::rcp_approx(d0), ptx::rcp_approx(d1))), a, b);
+}
+
 struct WaitCtx {
   volatile uint32_t* abort_flag;  // CTA-local
   int* status;                    // device-wide sticky status
@@ -321,13 +337,16 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
     ++xphase;
     return got;
   };
+  // With a softcap S holds tanh(s * cap_in) and the exponent step multiplies by
+  // cap_out (the softcap in log2 units); otherwise S stays in raw q.k units.  The
+  // ALiBi penalty is applied in the units S is held in.
   const bool capped = kMod && p.cap_in > 0.f;
-  const float sl2 = capped ? 1.0f : p.scale_log2;
+  const float sl2 = capped ? p.cap_out : p.scale_log2;
   float slope_s = 0.f;
   if constexpr (kMod) {
     if (p.alibi != nullptr) {
       const float a = p.alibi[(bh_t / p.H) * p.alibi_bstride + bh_t % p.H];
-      slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
+      slope_s = a * (1.4426950408889634f / sl2);
     }
   }
   const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
@@ -353,7 +372,11 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
     if constexpr (kMod) {
       if (capped) {
 #pragma unroll
-        for (int c = 0; c < kC; ++c) s[c] = p.cap_out * tanh_ex2(s[c] * p.cap_in);
+        for (int c = 0; c < kC; c += 2) {
+          ptx::unpack_f32x2(ptx::fmul2(ptx::pack_f32x2(s[c], s[c + 1]), ptx::pack_f32x2(p.cap_in, p.cap_in)),
+                            s[c], s[c + 1]);
+          tanh2_ex2(s[c], s[c + 1]);
+        }
       }
       if (slope_s != 0.f) {
         const float d0 = static_cast<float>(keyh - row);
