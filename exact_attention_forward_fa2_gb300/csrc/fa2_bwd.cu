@@ -1,5 +1,7 @@
 // Instantiation and launch of the backward kernels (bf16, head dim 64 and 128):
 // preprocess, then the dK/dV pass, then the dQ pass, all on the caller's stream.
+#include <atomic>
+
 #include "fa2_bwd_kernel.cuh"
 
 namespace fa2 {
@@ -7,13 +9,13 @@ namespace fa2 {
 namespace {
 
 template <class C, bool kCausal>
-cudaError_t launch_dkdv(BwdLaunch& L, bool& attr_done) {
+cudaError_t launch_dkdv(BwdLaunch& L, std::atomic<bool>& attr_done) {
   using Lay = DkvLayout<C>;
-  if (!attr_done) {
+  if (!attr_done.load(std::memory_order_acquire)) {  // idempotent: a race only repeats it
     const cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<C, kCausal>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done.store(true, std::memory_order_release);
   }
   const dim3 grid(static_cast<unsigned>(L.params.BHkv * L.params.n_ktiles));
   bwd_dkdv_kernel<C, kCausal><<<grid, C::kThreads, Lay::kSmemBytes, L.stream>>>(
@@ -22,12 +24,12 @@ cudaError_t launch_dkdv(BwdLaunch& L, bool& attr_done) {
 }
 
 template <class C, bool kCausal>
-cudaError_t launch_dq(BwdLaunch& L, bool& attr_done) {
-  if (!attr_done) {
+cudaError_t launch_dq(BwdLaunch& L, std::atomic<bool>& attr_done) {
+  if (!attr_done.load(std::memory_order_acquire)) {  // idempotent: a race only repeats it
     const cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<C, kCausal>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done.store(true, std::memory_order_release);
   }
   const int pairs = (L.params.n_qtiles + C::kQT - 1) / C::kQT;
   const dim3 grid(static_cast<unsigned>(L.params.BH * pairs));
@@ -39,7 +41,7 @@ cudaError_t launch_dq(BwdLaunch& L, bool& attr_done) {
 template <int D>
 cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
   using C = BwdCfg<D, D == 64 ? 8 : 4>;  // deeper ring at D = 64 (keeps one CTA per SM)
-  static bool attr[64][4] = {};
+  static std::atomic<bool> attr[64][4] = {};
   const int64_t rows_pad = static_cast<int64_t>(L.params.BH) * L.params.Mpad;
   const int64_t need = (rows_pad + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
@@ -48,7 +50,7 @@ cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
       L.params.M, L.params.Mpad, rows_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  bool* a = attr[dev];
+  std::atomic<bool>* a = attr[dev];
   e = L.causal ? launch_dkdv<C, true>(L, a[1]) : launch_dkdv<C, false>(L, a[0]);
   if (e != cudaSuccess) return e;
   using CQ = DqCfg<D, D == 64 ? 4 : 3>;  // two query tiles per CTA; K/V ring as deep as fits

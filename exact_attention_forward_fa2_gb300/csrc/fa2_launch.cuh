@@ -2,6 +2,8 @@
 // head dim) includes this file and calls launch_cfg with its tile configuration.
 #pragma once
 
+#include <atomic>
+
 #include "fa2_fwd_kernel.cuh"
 
 namespace fa2 {
@@ -9,13 +11,14 @@ namespace fa2 {
 // Sets the dynamic shared-memory limit once per device and kernel, then launches
 // one CTA per (work unit, key split) on the caller's stream.
 template <class C, bool kCausal, bool kMod, bool kWin>
-cudaError_t launch_one(FwdLaunch& L, bool& attr_done) {
-  if (!attr_done) {
+cudaError_t launch_one(FwdLaunch& L, std::atomic<bool>& attr_done) {
+  if (!attr_done.load(std::memory_order_acquire)) {
+    // setting the limit is idempotent, so threads that race here only repeat it
     const cudaError_t e = cudaFuncSetAttribute(fa2_fwd_kernel<C, kCausal, kMod, kWin>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done.store(true, std::memory_order_release);
   }
   const dim3 grid(static_cast<unsigned>(L.params.num_units * L.params.num_splits));
   const dim3 block(C::kThreads);
@@ -32,7 +35,7 @@ cudaError_t launch_one(FwdLaunch& L, bool& attr_done) {
 template <class C>
 cudaError_t launch_cfg(FwdLaunch& L) {
   using CH = FwdCfg<C::D, C::kBF16, C::kQTiles, C::kStages, 2>;
-  static bool attr_done[64][10] = {};
+  static std::atomic<bool> attr_done[64][10] = {};
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -44,7 +47,7 @@ cudaError_t launch_cfg(FwdLaunch& L) {
     L.params.units_per_head = (L.params.M + C::kQTiles * C::BM - 1) / (C::kQTiles * C::BM);
     L.params.num_units = L.params.units_per_head * L.params.BH;
   }
-  bool* done = attr_done[dev];
+  std::atomic<bool>* done = attr_done[dev];
   // kWin: spans and masks of a sliding window; kMod: softcap or ALiBi scores
   if (L.mod && L.params.cap_in > 0.f) {
     if (L.win)
