@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import subprocess
 import sys
@@ -231,6 +232,24 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ------------------------------------------------------------------ CPU oracle
+def cpu_model() -> str:
+    """Best-effort name of the host CPU (x86 lists a model name; Arm lists the
+    implementer and part numbers)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model Name", "Hardware"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", info, flags=re.M)
+        if m:
+            return m.group(1).strip()
+    imp = re.search(r"^CPU implementer\s*:\s*(\S+)", info, flags=re.M)
+    part = re.search(r"^CPU part\s*:\s*(\S+)", info, flags=re.M)
+    if imp and part:
+        return f"{platform.machine()} (CPU implementer {imp.group(1)}, part {part.group(1)})"
+    return platform.machine()
+
+
 def oracle_sample(w, q, k, v, seconds_target: float, seed: int = 0, n_start: int = 64):
     """Time the fp64 oracle on a bounded, seeded sample of the workload's rows,
     growing the sample from ``n_start`` rows until it takes ``seconds_target``.
@@ -320,7 +339,7 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "pass": args.pass_, "B": w.B, "H": w.H, "H_kv": w.Hkv, "M": w.M,
                    "N": w.N, "D": w.D, "causal": w.causal},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
                          "sample": (f"per step: {per_step[-1][1]} whole query heads of the workload "
                                     f"(fp64 backward), >= {per_step_s:.2f} s of CPU work" if bwd else
                                     f"per step: {per_step[-1][1]} seeded random query rows of the "
@@ -615,12 +634,12 @@ def run_ours(args, rank, local, world):
     }
     if args.cpu_baseline and bwd:
         tf, n, dt, cores = oracle_sample_bwd(w, q, k, v, seconds_target=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
                                 "sample": f"fp64 backward of {n} whole query heads of the workload "
                                           f"in {dt:.1f} s"}
     elif args.cpu_baseline:
         tf, n, dt, cores = oracle_sample(w, q, k, v, seconds_target=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": cores, "cpu": cpu_model(), "kind": "oracle",
                                 "sample": f"{n} seeded random query rows of the workload (fp64, all "
                                           f"their visible keys) in {dt:.1f} s"}
     print(json.dumps(line), flush=True)
