@@ -28,7 +28,9 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of this device's copy of the scratch array.  In host code the
 // array's name is only a stand-in for the symbol; the address must be asked for,
-// once per device, with that device current.
+// once per device, with that device current.  It stays valid for the life of the
+// device's primary context: a cudaDeviceReset ends that context, and with it the
+// address cached here (and every other per-device state the library keeps).
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA2_ERR_CUDA;
@@ -49,20 +51,14 @@ extern "C" int fa2_fwd_splitkv_noalloc(const void* q, const void* k, const void*
                                        float* lse, int B, int H, int H_kv, int M, int N, int D,
                                        float scale, int causal, int dtype, int num_splits,
                                        void* stream) {
-  if (num_splits <= 0) {
-    num_splits = fa2_splitkv_num_splits(B, H, H_kv, M, N, D, dtype);
-    if (num_splits < 0) return num_splits;
-  }
-  // The partials must fit in the built-in buffer; refuse rather than overflow it.
-  if (num_splits > 1 && fa2_splitkv_workspace_bytes(B, H, M, D, num_splits) > kScratchBytes)
-    return FA2_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (num_splits > 1) {
-    const int rc = scratch_for_current_device(&scratch);
-    if (rc != FA2_OK) return rc;
-  }
-  // Every slice writes each of its partial rows before the combine kernel reads
-  // it, so nothing left in the buffer by an earlier call needs clearing.
+  const int rc = scratch_for_current_device(&scratch);
+  if (rc != FA2_OK) return rc;
+  // fa2_fwd_splitkv lowers num_splits first (auto choice, the 64-slice cap, no
+  // empty slice) and then refuses, with FA2_ERR_WORKSPACE, a split whose partials
+  // need more than the buffer holds: exactly the calls that do not fit.  Every
+  // slice writes each of its partial rows before the combine kernel reads it, so
+  // nothing left in the buffer by an earlier call needs clearing.
   return fa2_fwd_splitkv(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, causal, dtype, num_splits,
-                         scratch, num_splits > 1 ? kScratchBytes : 0, stream);
+                         scratch, kScratchBytes, stream);
 }

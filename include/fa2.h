@@ -29,6 +29,12 @@
  *   - Errors are returned as negative status codes; nothing is launched on
  *     error.  No exception crosses the ABI and the library never exits the
  *     process.  fa2_strerror() names each code.
+ *   - The first call on a device sets up per-device state that later calls
+ *     reuse (the device address of the status word, the host-buffer entries'
+ *     copy streams, the built-in buffer of fa2_fwd_splitkv_noalloc).  It belongs
+ *     to the device's primary context: after a cudaDeviceReset of that device the
+ *     state is stale, and the library must not be used on it again in the same
+ *     process.
  */
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
@@ -131,16 +137,21 @@ size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits);
  * library's device code holds until the process exits.  This call allocates
  * nothing.  The pages have no counterpart to it; it is an interface addition.
  *
- * Arguments as fa2_fwd_splitkv, without the workspace.  Limit: the partials,
- * fa2_splitkv_workspace_bytes(B, H, M, D, num_splits) bytes, must fit in the
+ * Arguments as fa2_fwd_splitkv, without the workspace.  Limit: the partials of
+ * the split actually run (num_splits after fa2_fwd_splitkv lowers it: the
+ * automatic choice for <= 0, at most 64 and at most ceil(N/128) slices) take
+ * fa2_splitkv_workspace_bytes(B, H, M, D, that count) bytes and must fit in the
  * 32 MiB buffer, else FA2_ERR_WORKSPACE is returned and nothing runs (pass a
  * smaller num_splits, or use fa2_fwd_splitkv with your own workspace).
  * The first call on a device, with that device current, looks up the buffer's
  * device address (and may load the library's device code); make that first call
- * before any stream capture.  All calls on a device share the one buffer, which
- * keeps the previous call's contents (nothing in it needs to start at zero):
- * calls whose kernels may overlap on the GPU (different streams without
- * ordering, or several threads) race on it and must be serialised by the caller.
+ * before any stream capture.  The address is cached for the device's primary
+ * context: after a cudaDeviceReset the library's per-device state, this address
+ * included, is stale and the library must not be used on that device again in
+ * the same process.  All calls on a device share the one buffer, which keeps the
+ * previous call's contents (nothing in it needs to start at zero): calls whose
+ * kernels may overlap on the GPU (different streams without ordering, or several
+ * threads) race on it and must be serialised by the caller.
  */
 int fa2_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int H_kv, int M, int N, int D, float scale, int causal,

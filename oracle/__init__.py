@@ -71,6 +71,8 @@ def _bind(lib):
     lib.oracle_attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                         dbl, i32, i32]
     lib.oracle_attn_bwd_gqa.restype = i32
+    lib.oracle_omp_threads.argtypes = []
+    lib.oracle_omp_threads.restype = i32
     return lib
 
 
@@ -86,6 +88,12 @@ def _prep(q, k, v, gqa=False):
     B, H, M, D = q.shape
     N = k.shape[2]
     return q, k, v, B, H, M, N, D, _DTYPE_CODE[q.dtype]
+
+
+def omp_threads(lib=None) -> int:
+    """Threads the oracle's OpenMP regions run with in this process."""
+    lib = lib or load()
+    return int(lib.oracle_omp_threads())
 
 
 def attn_fwd(q, k, v, scale: float, causal: bool, lib=None):

@@ -41,6 +41,7 @@
  * -3 if a row had no visible key (cannot happen for N >= 1).
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -475,3 +476,7 @@ int oracle_attn_fwd_rows(const void* q, const void* k, const void* v,
   return oracle_attn_fwd_gqa_rows(q, k, v, rows, nrows, o, lse, B, H, H, M, N, D, scale,
                                   causal, dtype);
 }
+
+/* Threads an OpenMP parallel region of the entry points above runs with (the
+ * count the CPU baseline reports; it changes no arithmetic). */
+int oracle_omp_threads(void) { return omp_get_max_threads(); }

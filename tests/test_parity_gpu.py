@@ -1,22 +1,21 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle on
 the same seeded inputs.  Bar: |dL| <= 1e-2 for bf16 and <= 5e-3 for fp32
-inputs (TF32 tensor-core products); |dO| within the same bound on top of the
-rounding of the exact O to the output type (half a bf16 ulp of O; see
-gpu_helpers.compare), over every compared element.
+inputs (TF32 tensor-core products); |dO| <= the same bound on every element,
+except that bf16 outputs with |O_ref| >= 2 get half a bf16 ulp of O_ref on top
+(the error of storing the exact O in bf16; see gpu_helpers.o_bound).
 
 Shapes cover several 128-row tiles with ragged tails on both axes, the pages'
 test shapes ("FlashAttention-2 from PyTorch to Triton", the test file; "Writing
 FlashAttention 2 in Triton", numerics harness), degenerate sizes (one query,
-one key), non-square causal in both directions, and the five full-size
-workloads (full oracle comparison where the oracle finishes in seconds,
-sampled rows for the 8192 x 8192 ones).
+one key), non-square causal in both directions, and every full-size workload,
+compared with the oracle on every row.
 """
 import numpy as np
 import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_helpers import TOL, compare, sample_rows, to_device, to_host_f64
+from gpu_helpers import TOL, compare, compare_stats, record_parity, sample_rows, to_device, to_host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -118,17 +117,25 @@ def ramp_inputs(seed, B, H, M, N, D, dtype, sigma, lo, hi):
 @pytest.mark.parametrize("D", [64, 128])
 def test_rising_row_max(fa2, D):
     """Row maxima that rise over the key tiles (to ~38 in log2 units): a lagging
-    exponent base, and base moves with O rescales, against the oracle.  bf16 only:
-    the softmax code is the same for both input types, and TF32 products carry a
-    score error that grows with the score (the tensor core keeps 10 mantissa bits
-    of each fp32 operand).  On an fp32 version of these inputs (sigma 1.5, keys
-    scaled up to 2x, D = 64) the fp64 oracle run on Q and K truncated to TF32
-    already differs from the exact L by 0.0148, past the fp32 bound of 5e-3,
-    whatever the kernel does with the exponent base."""
+    exponent base, and base moves with O rescales, against the oracle.  The fp64
+    lagging recurrence (test_readings_cpu) run on the same inputs confirms that
+    rows move their base after the first key tile in both arms, so the kernels'
+    rescale branch is exercised.  The causal arm has M = N so that late rows see
+    the steep end of the ramp.  bf16 only: the softmax code is the same for both
+    input types, and TF32 products carry a score error that grows with the score
+    (the tensor core keeps 10 mantissa bits of each fp32 operand).  On an fp32
+    version of these inputs (sigma 1.5, keys scaled up to 2x, D = 64) the fp64
+    oracle run on Q and K truncated to TF32 already differs from the exact L by
+    0.0148, past the fp32 bound of 5e-3, whatever the kernel does with the
+    exponent base."""
+    from test_readings_cpu import lagging_recurrence
     dtype = si.BF16
-    B, H, M, N = 1, 2, 300, 1500
-    q, k, v = ramp_inputs(7, B, H, M, N, D, dtype, 2.0, 0.1, 2.5)
-    for causal in (False, True):
+    for causal, (B, H, M, N) in ((False, (1, 2, 300, 1500)), (True, (1, 2, 1500, 1500))):
+        q, k, v = ramp_inputs(7, B, H, M, N, D, dtype, 2.0, 0.1, 2.5)
+        # base moves past each row's first tile, head 0, by the fp64 recurrence
+        f64 = lambda a: si.bf16_bits_to_f32(a[0, 0]).astype(np.float64)
+        _, _, moves = lagging_recurrence(f64(q), f64(k), f64(v), D ** -0.5, causal)
+        assert moves > M, (causal, moves)
         o, lse = run_gpu(fa2, q, k, v, D ** -0.5, causal)
         o_ref, l_ref = oracle.attn_fwd(q, k, v, D ** -0.5, causal)
         eo, el, excess = compare(o, lse, o_ref, l_ref, dtype)
@@ -321,6 +328,7 @@ def test_split_kv_matches_unsplit_closely(fa2):
 
 
 def full_or_sampled(fa2, name, sampled):
+    import time
     w = si.WORKLOADS[name]
     q, k, v = si.make_qkv(w)
     if w.split_kv:
@@ -328,8 +336,10 @@ def full_or_sampled(fa2, name, sampled):
         to, tl = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=w.scale, causal=w.causal)
         torch.cuda.synchronize()
         o, lse = to_host_f64(to), tl.cpu().numpy().astype(np.float64)
+        del tq, tk, tv, to, tl
     else:
         o, lse = run_gpu(fa2, q, k, v, w.scale, w.causal)
+    t0 = time.perf_counter()
     if sampled:
         rows = sample_rows(w.B, w.H, w.M, w.N, w.causal)
         o_ref, l_ref = oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
@@ -337,21 +347,25 @@ def full_or_sampled(fa2, name, sampled):
     else:
         o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, w.scale, w.causal)
         o_cmp, l_cmp = o, lse
-        # every row was written: nothing left at a sentinel, all finite
-    eo, el, excess = compare(o_cmp, l_cmp, o_ref, l_ref, w.dtype)
+    oracle_s = time.perf_counter() - t0
+    # every row was written: nothing left at a sentinel, all finite
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    print(f"{name}: max|dO|={eo:.3e} max|dL|={el:.3e} excess over bound={excess:.3e}")
-    assert excess <= 0 and el <= TOL[w.dtype], (eo, el)
+    st = compare_stats(o_cmp, l_cmp, o_ref, l_ref, w.dtype)
+    record_parity(name, st, rows_compared="sampled" if sampled else "all", oracle_s=round(oracle_s, 1))
+    print(f"{name}: max|dO|={st['max_do']:.3e} (|O_ref|<2: {st['max_do_small']:.3e}, "
+          f">=2: {st['max_do_large']:.3e} on {st['n_large']} elements) max|dL|={st['max_dl']:.3e} "
+          f"max|O_ref|={st['max_abs_oref']:.3f} excess over bound={st['excess']:.3e} "
+          f"oracle {oracle_s:.1f} s")
+    assert st["excess"] <= 0 and st["max_dl"] <= TOL[w.dtype], st
 
 
+# Every workload of the pages' table, and the added ones, on every row: the
+# oracle takes about 30 s on 16 host cores for the largest (1.1e12 fp64 FLOP).
 @pytest.mark.parametrize("name", ["fp32_1x1x128x128x64", "tf32_4x12x2048x2048x64",
                                   "bf16_4x16x4096x4096x64_causal", "bf16_8x32x1000x3000x128_sharp",
+                                  "bf16_2x16x8192x8192x128", "bf16_2x16x8192x8192x128_causal",
+                                  "bf16_2x32x8192x8192x128_gqa8_causal",
                                   "bf16_1x32x128x32768x128_gqa8_splitkv", "bf16_16x32x1x8192x128_gqa8_decode"])
 def test_workload_full(fa2, name):
     full_or_sampled(fa2, name, sampled=False)
 
-
-@pytest.mark.parametrize("name", ["bf16_2x16x8192x8192x128", "bf16_2x16x8192x8192x128_causal",
-                                  "bf16_2x32x8192x8192x128_gqa8_causal"])
-def test_workload_sampled_rows(fa2, name):
-    full_or_sampled(fa2, name, sampled=True)

@@ -5,10 +5,13 @@ row max.
 "From FlashAttention to FlashAttention 2" (FlashAttention 2: What Changed) and
 "Writing FlashAttention 2 in Triton" (Step 3) move the running max m on every key
 tile and rescale the accumulator by exp(m_old - m_new).  The kernels move a row's
-base only when its max has grown past the base by more than 2^24 (log2 units).
+base only when its max has grown past the base by more than 24 in log2 units (a
+factor of 2^24).
 Here that lagging recurrence, written out in fp64 over 128-key tiles, is compared
 with the fp64 oracle (the two-pass definition) on rows whose max climbs over the
-tiles, so the base both lags and moves.
+tiles, so the base both lags and moves.  Two broken variants (no rescale of
+what was summed when the base moves; L without the base) must miss the oracle by
+far more than the 1e-12 the correct one meets, so the check can tell them apart.
 """
 import math
 
@@ -21,8 +24,9 @@ LAG_LOG2 = 24.0
 BN = 128
 
 
-def lagging_recurrence(q, k, v, scale, causal):
-    """O and L (natural log) of one head, tile by tile, with a lagging base."""
+def lagging_recurrence(q, k, v, scale, causal, rescale=True, base_in_l=True):
+    """O and L (natural log) of one head, tile by tile, with a lagging base.
+    ``rescale=False`` or ``base_in_l=False`` drop one step (test mutants)."""
     M, D = q.shape
     N = k.shape[0]
     c = scale / math.log(2.0)  # scores in log2 units
@@ -39,15 +43,16 @@ def lagging_recurrence(q, k, v, scale, causal):
             m_tile = float(s.max())
             if m_tile - base > LAG_LOG2:  # move the base; rescale what was summed
                 alpha = 0.0 if base == -math.inf else 2.0 ** (base - m_tile)
-                acc *= alpha
-                l *= alpha
+                if rescale:
+                    acc *= alpha
+                    l *= alpha
                 base = m_tile
                 moves += 1
             p = 2.0 ** (s - base)
             l += float(p.sum())
             acc += p @ v[j0:j1]
         o[i] = acc / l
-        lse[i] = (base + math.log2(l)) * math.log(2.0)
+        lse[i] = ((base if base_in_l else 0.0) + math.log2(l)) * math.log(2.0)
     return o, lse, moves
 
 
@@ -67,3 +72,8 @@ def test_lagging_base_matches_two_pass(causal):
     assert moves > M  # some rows moved their base after the first tile
     assert np.max(np.abs(o - o_ref[0, 0])) < 1e-12
     assert np.max(np.abs(lse - l_ref[0, 0])) < 1e-12
+    # a recurrence that forgets to rescale, or an L without the base, is caught
+    o_bad, l_bad, _ = lagging_recurrence(q, k, v, scale, causal, rescale=False)
+    assert max(np.max(np.abs(o_bad - o_ref[0, 0])), np.max(np.abs(l_bad - l_ref[0, 0]))) > 1e-3
+    o_bad, l_bad, _ = lagging_recurrence(q, k, v, scale, causal, base_in_l=False)
+    assert np.max(np.abs(l_bad - l_ref[0, 0])) > 1.0

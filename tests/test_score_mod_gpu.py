@@ -1,8 +1,8 @@
 """GPU parity of the score modifiers (fa2_fwd_ext: sliding window, softcap,
 ALiBi) against the fp64 oracle's attn_fwd_mod on the same seeded inputs.
 
-Same bar as the plain forward (|dL| <= 1e-2 bf16 / 5e-3 fp32; |dO| within that
-plus half a bf16 ulp of O for bf16 outputs).  Rows that a window leaves without
+Same bar as the plain forward (|dL| <= 1e-2 bf16 / 5e-3 fp32; |dO| within the
+same bound, plus half a bf16 ulp of O_ref for bf16 outputs with |O_ref| >= 2).  Rows that a window leaves without
 any visible key must come back as O = 0 exactly and L = -inf on both sides.
 Shapes span several 128-row tiles with ragged tails, windows whose edges cut
 through tiles, whole query tiles with no visible key, grouped-query heads, and
@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_helpers import TOL, compare, sample_rows, to_device, to_host_f64
+from gpu_helpers import TOL, compare, compare_stats, record_parity, to_device, to_host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -149,9 +149,10 @@ def test_no_modifier_matches_plain_forward_bitwise(fa2):
 
 
 @pytest.mark.parametrize("name", [n for n, w in si.WORKLOADS.items() if w.modified])
-def test_modifier_workload_sampled_rows(fa2, name):
+def test_modifier_workload_all_rows(fa2, name):
     """The modifier workloads at full size (8192 x 8192, D = 128), in the call the
-    bench times, on sampled rows."""
+    bench times, on every row."""
+    import time
     w = si.WORKLOADS[name]
     q, k, v = si.make_qkv(w)
     tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
@@ -160,9 +161,15 @@ def test_modifier_workload_sampled_rows(fa2, name):
     o, lse = fa2.fa2_fwd_ext(tq, tk, tv, scale=w.scale, causal=w.causal, window=w.window,
                              softcap=w.softcap, alibi_slopes=ts, num_splits=1)
     torch.cuda.synchronize()
-    rows = sample_rows(w.B, w.H, w.M, w.N, w.causal, n_random=1024)
-    og = to_host_f64(o).reshape(-1, w.D)[rows]
-    lg = lse.cpu().numpy().astype(np.float64).reshape(-1)[rows]
+    og = to_host_f64(o)
+    lg = lse.cpu().numpy().astype(np.float64)
+    t0 = time.perf_counter()
     orf, lrf = oracle.attn_fwd_mod(q, k, v, float(np.float32(w.scale)), w.causal, w.window, w.softcap,
-                                   slopes.astype(np.float64) if w.alibi else None, rows=rows)
+                                   slopes.astype(np.float64) if w.alibi else None)
+    oracle_s = time.perf_counter() - t0
     check(og, lg, orf, lrf, w.dtype, name)
+    seen = ~np.isneginf(lrf)
+    st = compare_stats(og[seen], lg[seen], orf[seen], lrf[seen], w.dtype)
+    record_parity(name, st, rows_compared="all", oracle_s=round(oracle_s, 1))
+    print(f"{name}: max|dO|={st['max_do']:.3e} (|O_ref|<2: {st['max_do_small']:.3e}) "
+          f"max|dL|={st['max_dl']:.3e} max|O_ref|={st['max_abs_oref']:.3f} oracle {oracle_s:.1f} s")
