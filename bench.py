@@ -641,7 +641,10 @@ def run_ours(args, rank, local, world):
     peak, hbm_peak, peak_kind = measured_peaks()
     peak_kind = f"bf16 dense burst, {peak_kind}"
     tf32_probe = None
-    if w.dtype != si.BF16:
+    if w.dtype != si.BF16 and not args.probes:
+        peak = TF32_OVER_BF16 * peak
+        peak_kind = "tf32 dense, nominal ratio x measured bf16 burst (the TF32 probe was skipped)"
+    elif w.dtype != si.BF16:
         # TF32 contraction: this GPU's TF32 rate, measured by a cuBLAS matmul probe
         tf32_probe = tf32_matmul_peak(dev)
         peak = tf32_probe
@@ -691,7 +694,7 @@ def run_ours(args, rank, local, world):
                    "protocol_median_of_100": protocol},
         "e2e": e2e,
         "sustained": sustained,
-        "sfu": None if bwd or w.dtype != si.BF16 else sfu_probe(fa2, local, 4.0 * w.D, peak),
+        "sfu": None if bwd or w.dtype != si.BF16 or not args.probes else sfu_probe(fa2, local, 4.0 * w.D, peak),
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks.summary(),
         "device_status": status,
@@ -731,6 +734,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-probes", dest="probes", action="store_false",
+                    help="skip the ex2-rate and TF32-peak probes after the timed steps (for launch lists)")
     ap.add_argument("--sustained-s", type=float, default=4.0,
                     help="seconds of back-to-back launches after the timed steps (0: skip)")
     ap.add_argument("--e2e-chunks", type=int, default=0,

@@ -119,6 +119,22 @@ bool pack_heads(int H, int H_kv, int M, int causal, bool use_mod) {
   return !use_mod && !causal && H / H_kv >= 2 && M < 128;
 }
 
+// Query heads per group of the causal launch order.  When the keys and values of
+// every head fit in half of L2 (kL2AllBytes) one group holds every head (the plain
+// longest-first order); otherwise a group holds as many whole key/value heads
+// (with their H / H_kv query heads) as fit in kL2GroupBytes, so that the CTAs in
+// flight (one group, and the start of the next) read K and V from L2.  Measured:
+// +0.8% on the 2 x 16 x 8192^2 x 128 causal workload (128 MiB of K/V, groups of
+// 8 heads), -1.1% on 4 x 16 x 4096^2 x 64 causal (64 MiB) if grouped there too.
+constexpr int64_t kL2AllBytes = int64_t(64) << 20;
+constexpr int64_t kL2GroupBytes = int64_t(32) << 20;
+int causal_head_group(int64_t bh, int group, int N, int D, int dtype) {
+  const int64_t kv_head_bytes = 2 * static_cast<int64_t>(N) * D * (dtype == FA2_BF16 ? 2 : 4);
+  if ((bh / group) * kv_head_bytes <= kL2AllBytes) return static_cast<int>(bh);
+  const int64_t kv_heads = std::max<int64_t>(1, kL2GroupBytes / kv_head_bytes);
+  return static_cast<int>(std::min<int64_t>(bh, kv_heads * group));
+}
+
 // CTAs of the forward before any key split.
 int64_t forward_units(int B, int H, int H_kv, int M, int qt) {
   if (pair_heads(H, H_kv, M, qt)) return static_cast<int64_t>(B) * H / 2;
@@ -230,6 +246,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
                         : nullptr;
   L.params.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   L.params.pair_heads = pair_heads(H, H_kv, M, qt) ? 1 : 0;
+  L.params.head_group = causal_head_group(bh, H / H_kv, N, D, dtype);
   // window bounds: an absent side widens to cover every key (row - M <= 0 and
   // row + N >= N - 1 for every row); causal caps the right side at the diagonal
   L.params.win_left = (mods.window_left < 0 || mods.window_left > M) ? M : mods.window_left;

@@ -58,6 +58,9 @@ struct FwdParams {
   // head (M <= 128 under grouped-query attention), instead of two query tiles of one
   // head, so that both tile slots of a CTA work and share the streamed K/V tiles
   int pair_heads;
+  // causal order: query heads per group (>= 1); a group's units all launch before
+  // the next group's, longest first within the group (see unit_of_block)
+  int head_group;
   // score modifiers.  Window (read by the kWin instantiations): key j is visible
   // to query row i iff i - win_left <= j <= i + win_right (the host folds the
   // causal bound into win_right and widens an unbounded side to cover every key).
@@ -74,12 +77,17 @@ struct FwdParams {
 // The exponent base of a row moves only when the row max has grown by more than
 // this many powers of two since the base was last set, so the O rescale (a TMEM
 // load and store of the whole accumulator row, on the path to the next P V) is
-// skipped on most tiles.  Any base gives the same O and L in exact arithmetic, and
-// rounding is relative, so the lag costs no precision; it bounds P by 2^24, l by
-// N 2^24 and the unnormalised O by N 2^24 max|v|, far inside the fp32 range.
-// With sharp score rows (scores of standard deviation 13 in log2 units) a bound of
-// 8 still moved the base of some row of a warp on 58% of key tiles, 24 on 6%.
-constexpr float kBaseLagLog2 = 24.0f;
+// skipped on tiles where the max grows little.  Any base gives the same O and L in
+// exact arithmetic, and it bounds P by 2^4, l by 16 N and the unnormalised O by
+// 16 N max|v|.  The bound is kept small for precision: a P is rounded to bf16
+// with a relative error of up to 2^-8 unless it is an exact power of two, and the
+// base equal to the row max makes the largest weight exactly 1; a base lagging by
+// up to 2^24 let the dominant weights of sharp rows (two keys of comparable score
+// and far-apart values) carry that rounding, and the worst |dO| on rows with
+// |O| < 2 of the sharp cross-attention workload rose from 8.7e-3 (bound 4) to
+// 1.03e-2 (bound 24).  On N(0, 1) scores the row max rarely grows by more than 4
+// after the first key tile, so the rescale stays rare there.
+constexpr float kBaseLagLog2 = 4.0f;
 
 // Device status codes (first failing wait site wins).
 enum : int {
@@ -174,8 +182,10 @@ struct Unit {
 };
 
 // Causal units are launched longest first (largest query offset, heads
-// interleaved) so the tail of the grid holds the short ones; non-causal units
-// keep one head's query tiles adjacent so its K/V stay hot in L2.
+// interleaved) so the tail of the grid holds the short ones, group of heads by
+// group of heads: the host sizes a group so that its keys and values fit in a
+// share of L2, so the CTAs in flight re-read K/V tiles from L2 instead of HBM.
+// Non-causal units keep one head's query tiles adjacent so its K/V stay hot in L2.
 __device__ __forceinline__ Unit unit_of_block(const FwdParams& p, bool causal, int b) {
   Unit u;
   if (p.pair_heads) {  // every unit is one tile long: any order
@@ -184,8 +194,13 @@ __device__ __forceinline__ Unit unit_of_block(const FwdParams& p, bool causal, i
     return u;
   }
   if (causal) {
-    u.pair = p.units_per_head - 1 - b / p.BH;
-    u.bh = b % p.BH;
+    const int per_group = p.head_group * p.units_per_head;
+    const int g = b / per_group;
+    const int r = b - g * per_group;
+    const int h0 = g * p.head_group;
+    const int gh = min(p.head_group, p.BH - h0);  // heads in this group (the last may be short)
+    u.pair = p.units_per_head - 1 - r / gh;
+    u.bh = h0 + r % gh;
   } else {
     u.bh = b / p.units_per_head;
     u.pair = b % p.units_per_head;
@@ -978,11 +993,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int ch = 0; ch < C::D / 32; ++ch) tmem_ld_x32(tO + ch * 32, o[ch]);
         if constexpr (C::kLOnes) tmem_ld_x16(tO + C::D, ol);
         tmem_ld_wait();
+        const uint64_t alpha2 = pack_f32x2(alpha, alpha);
 #pragma unroll
         for (int ch = 0; ch < C::D / 32; ++ch) {
           reg_fence_x32(o[ch]);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[ch][i] = __float_as_uint(__uint_as_float(o[ch][i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            float a, b;
+            unpack_f32x2(fmul2(pack_f32x2(__uint_as_float(o[ch][i]), __uint_as_float(o[ch][i + 1])), alpha2), a, b);
+            o[ch][i] = __float_as_uint(a);
+            o[ch][i + 1] = __float_as_uint(b);
+          }
           tmem_st_x32(tO + ch * 32, o[ch]);
         }
         if constexpr (C::kLOnes) {

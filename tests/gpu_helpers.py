@@ -1,5 +1,5 @@
-"""Helpers for the GPU parity tests: host arrays to device tensors and back,
-row sampling for full-size workloads, and the comparison against the oracle."""
+"""Helpers for the GPU parity tests: host arrays to device tensors and back, and
+the comparison against the oracle (the per-element bound and its statistics)."""
 from __future__ import annotations
 
 import numpy as np
@@ -23,27 +23,6 @@ def to_host_f64(t) -> np.ndarray:
         bits = t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
         return si.bf16_bits_to_f32(bits).astype(np.float64)
     return t.cpu().numpy().astype(np.float64)
-
-
-def sample_rows(B, H, M, N, causal, n_random=4096, seed=0, full_heads=((0, 0), (-1, -1))):
-    """Flat row indices (b*H+h)*M+i to check at full size: every row of the
-    first and last head, and in every head the first and last rows, rows at
-    and next to the 128-row tile edges that carry the causal diagonal, the
-    ragged-tail rows, plus seeded random rows."""
-    rows = set()
-    for b, h in full_heads:
-        bh = (b % B) * H + (h % H)
-        rows.update(range(bh * M, (bh + 1) * M))
-    edges = {0, 1, M - 1, M - 2}
-    for e in range(0, M, 128):
-        edges.update({e, e + 1, e + 127, e + 128, e - 1})
-    edges.update({M - 1 - (M % 128), (M // 128) * 128})
-    edges = [i for i in edges if 0 <= i < M]
-    for bh in range(B * H):
-        rows.update(bh * M + i for i in edges)
-    rng = np.random.default_rng(seed)
-    rows.update(rng.integers(0, B * H * M, size=n_random).tolist())
-    return np.array(sorted(rows), np.int64)
 
 
 def half_ulp_bf16(x: np.ndarray) -> np.ndarray:

@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_helpers import TOL, compare, compare_stats, record_parity, sample_rows, to_device, to_host_f64
+from gpu_helpers import TOL, compare, compare_stats, record_parity, to_device, to_host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -101,7 +101,7 @@ def test_sharp_scores_ragged(fa2):
 def ramp_inputs(seed, B, H, M, N, D, dtype, sigma, lo, hi):
     """Keys scaled by a factor rising linearly from lo to hi along the key axis,
     so every score row's max climbs from tile to tile: by small steps that the
-    kernel leaves in a lagging exponent base (up to 24 in log2 units) and across
+    kernel leaves in a lagging exponent base (up to 4 in log2 units) and across
     that bound, where the base moves and O is rescaled."""
     q = si.normal(seed, 1, (B, H, M, D), sigma, dtype)
     k = si.normal(seed, 2, (B, H, N, D), sigma, dtype)
@@ -327,7 +327,7 @@ def test_split_kv_matches_unsplit_closely(fa2):
     assert float((o1.float() - o2.float()).abs().max()) < 1e-2
 
 
-def full_or_sampled(fa2, name, sampled):
+def check_workload_all_rows(fa2, name):
     import time
     w = si.WORKLOADS[name]
     q, k, v = si.make_qkv(w)
@@ -340,18 +340,12 @@ def full_or_sampled(fa2, name, sampled):
     else:
         o, lse = run_gpu(fa2, q, k, v, w.scale, w.causal)
     t0 = time.perf_counter()
-    if sampled:
-        rows = sample_rows(w.B, w.H, w.M, w.N, w.causal)
-        o_ref, l_ref = oracle.attn_fwd_gqa_rows(q, k, v, w.scale, w.causal, rows)
-        o_cmp, l_cmp = o.reshape(-1, w.D)[rows], lse.reshape(-1)[rows]
-    else:
-        o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, w.scale, w.causal)
-        o_cmp, l_cmp = o, lse
+    o_ref, l_ref = oracle.attn_fwd_gqa(q, k, v, w.scale, w.causal)
     oracle_s = time.perf_counter() - t0
     # every row was written: nothing left at a sentinel, all finite
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    st = compare_stats(o_cmp, l_cmp, o_ref, l_ref, w.dtype)
-    record_parity(name, st, rows_compared="sampled" if sampled else "all", oracle_s=round(oracle_s, 1))
+    st = compare_stats(o, lse, o_ref, l_ref, w.dtype)
+    record_parity(name, st, rows_compared="all", oracle_s=round(oracle_s, 1))
     print(f"{name}: max|dO|={st['max_do']:.3e} (|O_ref|<2: {st['max_do_small']:.3e}, "
           f">=2: {st['max_do_large']:.3e} on {st['n_large']} elements) max|dL|={st['max_dl']:.3e} "
           f"max|O_ref|={st['max_abs_oref']:.3f} excess over bound={st['excess']:.3e} "
@@ -367,5 +361,5 @@ def full_or_sampled(fa2, name, sampled):
                                   "bf16_2x32x8192x8192x128_gqa8_causal",
                                   "bf16_1x32x128x32768x128_gqa8_splitkv", "bf16_16x32x1x8192x128_gqa8_decode"])
 def test_workload_full(fa2, name):
-    full_or_sampled(fa2, name, sampled=False)
+    check_workload_all_rows(fa2, name)
 

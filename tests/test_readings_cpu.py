@@ -5,8 +5,8 @@ row max.
 "From FlashAttention to FlashAttention 2" (FlashAttention 2: What Changed) and
 "Writing FlashAttention 2 in Triton" (Step 3) move the running max m on every key
 tile and rescale the accumulator by exp(m_old - m_new).  The kernels move a row's
-base only when its max has grown past the base by more than 24 in log2 units (a
-factor of 2^24).
+base only when its max has grown past the base by more than 4 in log2 units (a
+factor of 2^4).
 Here that lagging recurrence, written out in fp64 over 128-key tiles, is compared
 with the fp64 oracle (the two-pass definition) on rows whose max climbs over the
 tiles, so the base both lags and moves.  Two broken variants (no rescale of
@@ -20,7 +20,7 @@ import pytest
 
 import oracle
 
-LAG_LOG2 = 24.0
+LAG_LOG2 = 4.0  # the kernels' bound (kBaseLagLog2)
 BN = 128
 
 

@@ -2,7 +2,7 @@
 import numpy as np
 
 import seeded_inputs as si
-from gpu_helpers import TOL, compare, compare_stats, half_ulp_bf16, o_bound, sample_rows
+from gpu_helpers import TOL, compare, compare_stats, half_ulp_bf16, o_bound
 
 
 def test_half_ulp_bf16_values():
@@ -19,17 +19,6 @@ def test_half_ulp_bounds_bf16_rounding():
     # the bound is reached: rounding error of the exact value can exceed 1e-2 for |x| >= 4
     big = np.abs(x) >= 4
     assert np.max(np.abs(r - x)[big]) > 1e-2
-
-
-def test_sample_rows_cover_edges_and_stay_in_range():
-    B, H, M, N = 2, 3, 1000, 3000
-    rows = sample_rows(B, H, M, N, causal=False, n_random=100)
-    assert rows.min() >= 0 and rows.max() < B * H * M
-    assert set(range(M)) <= set(rows.tolist())                 # first head in full
-    assert set(range((B * H - 1) * M, B * H * M)) <= set(rows.tolist())  # last head in full
-    for bh in range(B * H):
-        for i in (0, M - 1, 127, 128, 895, 896, 999):
-            assert bh * M + i in set(rows.tolist())
 
 
 def test_o_bound_is_flat_below_two_and_adds_half_an_ulp_above():
