@@ -102,7 +102,8 @@ int encode_map(CUtensorMap* map, const void* ptr, int dtype, int D, int rows, in
 
 constexpr int kMaxSplits = 64;
 
-int64_t kv_tiles_total(int N) { return (static_cast<int64_t>(N) + 127) / 128; }
+// Key tiles of `bn` keys covering N keys.
+int64_t kv_tiles_total(int N, int bn) { return (static_cast<int64_t>(N) + bn - 1) / bn; }
 
 // Whether a unit pairs the single query tile of two heads that read the same
 // key/value head (two tile slots per CTA, M <= 128, an even number of query
@@ -143,10 +144,10 @@ int64_t forward_units(int B, int H, int H_kv, int M, int qt) {
 
 // Split count that fills about one wave of CTAs when the query tiles alone do
 // not: floor(#SMs / units), with at least 4 key tiles per split.
-int auto_splits(int64_t units, int N, int sms) {
+int auto_splits(int64_t units, int N, int bn, int sms) {
   if (units >= sms) return 1;
   int64_t s = sms / units;
-  s = std::min<int64_t>(s, kv_tiles_total(N) / 4);
+  s = std::min<int64_t>(s, kv_tiles_total(N, bn) / 4);
   return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(s, kMaxSplits)));
 }
 
@@ -199,10 +200,15 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   }
   const int64_t bh = static_cast<int64_t>(B) * H;
   const int64_t bh_kv = static_cast<int64_t>(B) * H_kv;
-  const int qt = fa2::qtiles_for(dtype == FA2_FP32, D);
+  // query tiles per CTA and keys per key/value tile of the kernel configuration that
+  // will run: softcap, sliding window or plain (see fa2_config.h)
+  const int cap_on = mods.softcap > 0.f ? 1 : 0;
+  const int win_on = (mods.window_left >= 0 || (!causal && mods.window_right >= 0)) ? 1 : 0;
+  const int qt = fa2::qtiles_for(dtype == FA2_FP32, D, cap_on, win_on);
   const int64_t units = forward_units(B, H, H_kv, M, qt);
   if (bh > INT_MAX || units > INT_MAX) return FA2_ERR_TOO_LARGE;
-  const int64_t n_kv = kv_tiles_total(N);
+  const int bn = fa2::kv_tile_for(dtype == FA2_FP32, D, cap_on, win_on);
+  const int64_t n_kv = kv_tiles_total(N, bn);
   int tiles_per_split = static_cast<int>(n_kv);
   if (num_splits > 1) {
     tiles_per_split = static_cast<int>((n_kv + num_splits - 1) / num_splits);
@@ -223,11 +229,11 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
 
   fa2::FwdLaunch L;
   rc = encode_map(&L.tmQ, q, dtype, D, M, bh);
-  if (rc == FA2_OK) rc = encode_map(&L.tmK, k, dtype, D, N, bh_kv);
+  if (rc == FA2_OK) rc = encode_map(&L.tmK, k, dtype, D, N, bh_kv, CU_TENSOR_MAP_SWIZZLE_128B, bn);
   // fp32 V is read MN-major as TF32: 32-byte-chunk swizzle (see the kernel header)
   if (rc == FA2_OK)
     rc = encode_map(&L.tmV, v, dtype, D, N, bh_kv,
-                    dtype == FA2_BF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
+                    dtype == FA2_BF16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B, bn);
   if (rc == FA2_OK) rc = encode_map(&L.tmO, o, dtype, D, M, bh);
   if (rc != FA2_OK) return rc;
   L.params.lse = lse;
@@ -257,7 +263,7 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   L.params.alibi = mods.alibi;
   L.params.alibi_bstride = mods.alibi_bstride;
   L.causal = causal ? 1 : 0;
-  L.win = (mods.window_left >= 0 || (!causal && mods.window_right >= 0)) ? 1 : 0;
+  L.win = win_on;
   L.mod = (mods.softcap > 0.f || mods.alibi != nullptr || L.win) ? 1 : 0;
   L.stream = static_cast<cudaStream_t>(stream);
 
@@ -340,7 +346,7 @@ extern "C" int fa2_splitkv_num_splits(int B, int H, int H_kv, int M, int N, int 
     M = (H / H_kv) * M;
     H = H_kv;
   }
-  return auto_splits(forward_units(B, H, H_kv, M, qt), N, sms);
+  return auto_splits(forward_units(B, H, H_kv, M, qt), N, fa2::kv_tile_for(dtype == FA2_FP32, D), sms);
 }
 
 extern "C" size_t fa2_splitkv_workspace_bytes(int B, int H, int M, int D, int num_splits) {

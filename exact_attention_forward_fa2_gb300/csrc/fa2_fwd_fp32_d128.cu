@@ -4,9 +4,12 @@
 
 namespace fa2 {
 
-using Cfg_fp32_d128 = FwdCfg<128, false, 1, 1>;
-static_assert(qtiles_for(1, 128) == Cfg_fp32_d128::kQTiles, "host and kernel tile configs differ");
+// the plain and ALiBi kernels, the sliding-window kernels (one softmax warpgroup
+// per query tile) and the softcap kernels (two per query tile)
+using Cfg_fp32_d128 = FwdCfg<128, false, qtiles_for(1, 128), 1, 1, kv_tile_for(1, 128)>;
+using CfgWin_fp32_d128 = FwdCfg<128, false, qtiles_for(1, 128, 0, 1), 1, 1, kv_tile_for(1, 128, 0, 1)>;
+using CfgCap_fp32_d128 = FwdCfg<128, false, qtiles_for(1, 128, 1), 1, 2, kv_tile_for(1, 128, 1)>;
 
-cudaError_t launch_fp32_d128(FwdLaunch& L) { return launch_cfg<Cfg_fp32_d128>(L); }
+cudaError_t launch_fp32_d128(FwdLaunch& L) { return launch_cfg<Cfg_fp32_d128, CfgWin_fp32_d128, CfgCap_fp32_d128>(L); }
 
 }  // namespace fa2

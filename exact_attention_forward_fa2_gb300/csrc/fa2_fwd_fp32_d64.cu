@@ -4,9 +4,12 @@
 
 namespace fa2 {
 
-using Cfg_fp32_d64 = FwdCfg<64, false, 2, 2>;
-static_assert(qtiles_for(1, 64) == Cfg_fp32_d64::kQTiles, "host and kernel tile configs differ");
+// the plain and ALiBi kernels, the sliding-window kernels (one softmax warpgroup
+// per query tile) and the softcap kernels (two per query tile)
+using Cfg_fp32_d64 = FwdCfg<64, false, qtiles_for(1, 64), 2, 1, kv_tile_for(1, 64)>;
+using CfgWin_fp32_d64 = FwdCfg<64, false, qtiles_for(1, 64, 0, 1), 2, 1, kv_tile_for(1, 64, 0, 1)>;
+using CfgCap_fp32_d64 = FwdCfg<64, false, qtiles_for(1, 64, 1), 2, 2, kv_tile_for(1, 64, 1)>;
 
-cudaError_t launch_fp32_d64(FwdLaunch& L) { return launch_cfg<Cfg_fp32_d64>(L); }
+cudaError_t launch_fp32_d64(FwdLaunch& L) { return launch_cfg<Cfg_fp32_d64, CfgWin_fp32_d64, CfgCap_fp32_d64>(L); }
 
 }  // namespace fa2

@@ -125,6 +125,35 @@ def test_large_softcap_at_saturation(fa2, causal):
     check(og, lg, orf, lrf, si.BF16, f"softcap 50 saturated, causal={causal}")
 
 
+@pytest.mark.parametrize("dtype,D", [(si.BF16, 128), (si.BF16, 64), (si.FP32, 64)])
+def test_softcap_error_on_single_key_rows(fa2, dtype, D):
+    """Window (0, 0) leaves row i one key, so L_i = c tanh(s_i / c) exactly, and the
+    error of the kernel's tanh, times the cap c, lands on L unchanged: the case a
+    sharp row with one dominant key approaches.  Scores s_i = scale q_i . k_i span
+    [-3c, 3c] with c = 50 (q_i = a_i e_0, k_i = e_0), so tanh is taken across its
+    whole range, the steep part included (q_i in bf16 precision, so TF32 products
+    are exact too)."""
+    M = N = 512
+    cap = 50.0
+    scale = 1.0 / math.sqrt(D)
+    # a_i exact in bf16 (hence in TF32 too), so the products carry no input rounding
+    a = si.bf16_bits_to_f32(si.f64_to_bf16_bits(np.linspace(-3 * cap, 3 * cap, M) / scale)).astype(np.float64)
+    q = np.zeros((1, 1, M, D))
+    q[0, 0, :, 0] = a
+    k = np.zeros((1, 1, N, D))
+    k[0, 0, :, 0] = 1.0
+    v = si.normal(395, 3, (1, 1, N, D), 1.0, si.FP64)
+    if dtype == si.BF16:
+        q, k, v = (si.f64_to_bf16_bits(x) for x in (q, k, v))
+    else:
+        q, k, v = (x.astype(np.float32) for x in (q, k, v))
+    tq, tk, tv = (to_device(x, DEV) for x in (q, k, v))
+    o, lse = fa2.fa2_fwd_ext(tq, tk, tv, scale=scale, window=(0, 0), softcap=cap)
+    torch.cuda.synchronize()
+    orf, lrf = oracle.attn_fwd_mod(q, k, v, float(np.float32(scale)), False, (0, 0), cap, None)
+    check(to_host_f64(o), lse.cpu().numpy().astype(np.float64), orf, lrf, dtype, f"single-key softcap D={D}")
+
+
 def test_one_key_window_returns_that_value_row(fa2):
     """window (0, 0): row i sees only key i, so O_i = V_i exactly (bf16 in and out)
     and L_i = scale q_i . k_i; rows past N see nothing."""
