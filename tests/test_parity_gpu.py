@@ -87,6 +87,25 @@ def test_small_shapes_all_rows(fa2, shape, causal, dtype):
     assert excess <= 0 and el <= TOL[dtype], (eo, el)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [111, 112, 113, 224, 225, 335])
+def test_key_tile_edges_bf16_d128(fa2, N, causal):
+    """bf16 at D = 128 streams keys in 112-key tiles: key counts on, just below and
+    just above the tile edges, against query tiles of 128 rows (so causal
+    diagonals cross two key tiles), through the plain and the split-KV entries."""
+    B, H, M, D = 1, 2, 260, 128
+    q, k, v = inputs(4000 + N, B, H, M, N, D, si.BF16)
+    o, lse = run_gpu(fa2, q, k, v, D ** -0.5, causal)
+    o_ref, l_ref = oracle.attn_fwd(q, k, v, D ** -0.5, causal)
+    eo, el, excess = compare(o, lse, o_ref, l_ref, si.BF16)
+    assert excess <= 0 and el <= TOL[si.BF16], (eo, el)
+    tq, tk, tv = (to_device(a, DEV) for a in (q, k, v))
+    os_, ls_ = fa2.fa2_fwd_splitkv(tq, tk, tv, scale=D ** -0.5, causal=causal, num_splits=3)
+    torch.cuda.synchronize()
+    eo, el, excess = compare(to_host_f64(os_), ls_.cpu().numpy().astype(np.float64), o_ref, l_ref, si.BF16)
+    assert excess <= 0 and el <= TOL[si.BF16], ("split", eo, el)
+
+
 def test_sharp_scores_ragged(fa2):
     """sigma_QK = 3: near one-hot rows that exercise the max rescaling."""
     B, H, M, N, D = 2, 3, 300, 777, 128
