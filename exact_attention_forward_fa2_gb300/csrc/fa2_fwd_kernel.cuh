@@ -20,9 +20,11 @@
 // Shared-memory tiles are written by TMA with a 128-byte swizzle; fp32 V tiles
 // (the B operand of P V, read MN-major as TF32) use the swizzle of 32-byte chunks
 // that the tensor core expects for 32-bit MN-major operands.
-// TMEM columns: S_t at [t*128, t*128+128) (P overwrites it in place), O_t at
-// [kQTiles*128 + t*D, ... + D).  With two query tiles the MMA warp alternates
-// between them, so one tile's softmax overlaps the other tile's two GEMMs.
+// TMEM columns: S_t at [t*BN, t*BN + BN) for key tiles of BN keys (P overwrites it
+// in place), O_t at [kQTiles*BN + t*W, ... + W), where W = D, or D + 16 when the
+// P V GEMM also forms the row sum from a ones block in V.  With two query tiles
+// the MMA warp alternates between them, so one tile's softmax overlaps the other
+// tile's two GEMMs.
 //
 // Every mbarrier wait is bounded in time; a wait that runs out records an error
 // code in a device status word, sets a CTA-local abort flag, and all roles wind
@@ -586,520 +588,495 @@ __device__ __forceinline__ void softmax_halves(const FwdParams& p, const CUtenso
   }
 }
 
+// One key tile of a query tile's online softmax, one warpgroup per tile (thread
+// r owns row r = TMEM lane r): S row from TMEM, score modifiers, mask, row max, the
+// exponent base (moved only past kBaseLagLog2), P = exp2(s*sl2 - base) rounded to
+// the P V operand type and written over S, the row sum (when the softmax forms
+// it), the rescale of O when the base moved, then the P barrier.  The caller has
+// waited for S (and fenced); key0 is the tile's first key, not_first is false on
+// a tile's first key tile of the item.
 template <class C, bool kCausal, bool kMod, bool kWin>
-__global__ void __launch_bounds__(C::kThreads, 1)
-    fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                   const FwdParams p) {
+__device__ __forceinline__ void softmax_step(const FwdParams& p, uint32_t tS, uint32_t tO, uint32_t pbar,
+                                             int key0, int tile_row0, int row, bool capped, float slope_s,
+                                             float sl2, uint64_t sl2x2, bool not_first, float& m_run,
+                                             float& l_run) {
   using namespace ptx;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::kOffMisc);
-  // misc[0] TMEM base address, misc[1] abort flag, misc[2] status at CTA start
-
-  const int warp = static_cast<int>(threadIdx.x) / 32;
-  const int lane = static_cast<int>(threadIdx.x) % 32;
-  auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
-
-  const int split = static_cast<int>(blockIdx.x) % p.num_splits;
-  const int kb = split * p.tiles_per_split;  // first key tile of this CTA's split
-  const Unit unit = unit_of_block(p, kCausal, static_cast<int>(blockIdx.x) / p.num_splits);
-  const int bh = unit.bh;
-  // key/value head read by this query head (grouped-query attention, "From
-  // FlashAttention to FlashAttention 2", Layer 8: h_kv = h / (H / H_kv))
-  const int bh_kv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
-  // Query tile t visits key tiles [kt0[t], kt0[t] + nkv[t]); the CTA streams key
-  // tiles ks, ks + 1, ..., ks + n_max - 1 and tile t uses stream positions
-  // [jb[t], jb[t] + nkv[t]).  Without a window every tile starts at the split's
-  // first key tile, so jb is 0.
-  int row0[C::kQTiles], kt0[C::kQTiles], nkv[C::kQTiles], jb[C::kQTiles];
-  int ks = kb, n_max = 0;
+  tc_fence_after_sync();
+  // the whole S row of this thread: every TMEM load in flight, one wait (32
+  // columns per load; a 112-key row ends with a 16-column load)
+  constexpr int kLd = (C::BN + 31) / 32;
+  uint32_t v[kLd][32];
 #pragma unroll
-  for (int t = 0; t < C::kQTiles; ++t) {
-    row0[t] = tile_first_row(p, unit, t, C::kQTiles);
-    const KvSpan sp = kv_span<kWin, C::BN>(row0[t], p, kCausal, split);
-    kt0[t] = sp.first;
-    nkv[t] = sp.count;
-    jb[t] = 0;
-    n_max = max(n_max, nkv[t]);
+  for (int ch = 0; ch < C::BN / 32; ++ch) tmem_ld_x32(tS + ch * 32, v[ch]);
+  if constexpr (C::BN % 32 == 16)
+    tmem_ld_x16(tS + (C::BN / 32) * 32, *reinterpret_cast<uint32_t(*)[16]>(&v[kLd - 1][0]));
+  tmem_ld_wait();
+#pragma unroll
+  for (int ch = 0; ch < C::BN / 32; ++ch) reg_fence_x32(v[ch]);
+  if constexpr (C::BN % 32 == 16) reg_fence_x16(*reinterpret_cast<uint32_t(*)[16]>(&v[kLd - 1][0]));
+  static_assert(C::BN % 32 == 0 || C::BN % 32 == 16, "S rows load in 32- and 16-column pieces");
+  float s[C::BN];
+#pragma unroll
+  for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
+  if constexpr (kMod) {
+    // score modifiers: softcap (into log2 units), then the ALiBi distance penalty
+    if (capped) {
+#pragma unroll
+      for (int c = 0; c < C::BN; ++c) s[c] = p.cap_out * tanh_mufu(s[c] * p.cap_in);
+    }
+    if (slope_s != 0.f) {
+      const float d0 = static_cast<float>(key0 - row);
+#pragma unroll
+      for (int c = 0; c < C::BN; ++c) s[c] = fmaf(-slope_s, fabsf(d0 + static_cast<float>(c)), s[c]);
+    }
   }
   if constexpr (kWin) {
-    int lo = 0x7fffffff, hi = 0;
+    // window mask, on tiles that cross N or either window edge of some row
+    const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||
+                          (key0 < tile_row0 + C::BM - 1 - p.win_left);
+    if (boundary) {
+      const int hi = min(p.N - 1, row + p.win_right) - key0;
+      const int lo = row - p.win_left - key0;
+#pragma unroll
+      for (int c = 0; c < C::BN; ++c) s[c] = (c >= lo && c <= hi) ? s[c] : -INFINITY;
+    }
+  } else {
+    // mask keys past N and, when causal, keys after this row (boundary tiles only)
+    const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
+    if (boundary) {
+      int lim = p.N - 1 - key0;
+      if (kCausal) lim = min(lim, row - key0);
+#pragma unroll
+      for (int c = 0; c < C::BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
+    }
+  }
+  // row max: four independent chains of 3-input max over s[4..BN-5], then the
+  // last four columns
+  float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+  for (int c = 4; c + 8 <= C::BN; c += 8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], s[c + q], s[c + 4 + q]);
+  }
+  static_assert(C::BN % 8 == 0, "the max chains cover s[0..3], pairs of 4, then s[BN-4..BN-1]");
+  static_assert(C::BN % 64 == 0 || C::BN % 64 == 48, "P is stored in pieces of 64 keys and one of 48");
+#pragma unroll
+  for (int q = 0; q < 4; ++q) mx[q] = fmaxf(mx[q], s[C::BN - 4 + q]);
+  const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+  const float m_new = fmaxf(m_run, m_tile);
+  // Move the exponent base only when the max grew by more than kBaseLagLog2:
+  // the result is exact for any base, and skipping the rescale keeps O in TMEM
+  // untouched on most tiles.  (-inf) - (-inf) is NaN, so an empty row stays put.
+  const bool rescale = (m_new - m_run) > kBaseLagLog2;
+  const float m_use = rescale ? m_new : m_run;
+  const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.0f;
+  const float neg_base = (m_use == -INFINITY) ? 0.f : -m_use;
+  const uint64_t nb2 = pack_f32x2(neg_base, neg_base);
+  // P = exp2(s*sl2 - base), rounded to the P.V operand type.  l sums the
+  // rounded values, so O = sum(P v) / sum(P) is an exact convex combination
+  // of V rows with the weights the tensor core actually used.
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // packed pairs of partial sums
+#pragma unroll
+  for (int h = 0; h < (C::BN + 63) / 64; ++h) {  // pieces of 64 keys (the last of a 112-key row: 48)
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int c = h * 64 + 2 * i;
+      if (c >= C::BN) break;
+      float x0, x1;
+      unpack_f32x2(ffma2(pack_f32x2(s[c], s[c + 1]), sl2x2, nb2), x0, x1);
+      const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if constexpr (C::kBF16) {
+        const uint32_t w = pack_bf16x2(p0, p1);
+        pk[i] = w;
+        if constexpr (!C::kLOnes)
+          acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(__uint_as_float(w << 16),
+                                                    __uint_as_float(w & 0xffff0000u)));
+      } else if constexpr (C::kLOnes) {
+        // fp32 P goes to TMEM as it is: the tensor core reads it as TF32 for the
+        // P V product and for the ones columns alike, so l is the sum of exactly
+        // the weights the product used (an explicit rounding measured 16% slower)
+        s[c] = p0;
+        s[c + 1] = p1;
+      } else {
+        const uint32_t r0 = round_tf32(p0), r1 = round_tf32(p1);
+        s[c] = __uint_as_float(r0);
+        s[c + 1] = __uint_as_float(r1);
+        acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(s[c], s[c + 1]));
+      }
+    }
+    if constexpr (C::kBF16) {
+      if (C::BN - h * 64 >= 64) {
+        tmem_st_x32(tS + h * 32, pk);  // 64 keys -> 32 columns of bf16x2
+      } else {                         // 48 keys -> 24 columns
+        tmem_st_x16(tS + h * 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st_x8(tS + h * 32 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&pk[16]));
+      }
+    } else {
+      uint32_t q0[32], q1[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        q0[i] = __float_as_uint(s[h * 64 + i]);
+        q1[i] = __float_as_uint(s[h * 64 + 32 + i]);
+      }
+      tmem_st_x32(tS + h * 64, q0);
+      tmem_st_x32(tS + h * 64 + 32, q1);
+    }
+  }
+  if constexpr (!C::kLOnes) {
+    float a0, a1, a2, a3, a4, a5, a6, a7;
+    unpack_f32x2(acc[0], a0, a1);
+    unpack_f32x2(acc[1], a2, a3);
+    unpack_f32x2(acc[2], a4, a5);
+    unpack_f32x2(acc[3], a6, a7);
+    l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
+  }
+  if (not_first && __any_sync(0xffffffffu, rescale)) {
+    // O_t *= alpha.  P_{j-1} V_{j-1} has landed: the MMA warp issued it before
+    // S_j, and a commit completes only after every earlier MMA.
+    tc_fence_after_sync();
+    // every load of the row in flight at once, one wait
+    uint32_t o[C::D / 32][32];
+    uint32_t ol[16];  // the row sum columns, which scale with O
+#pragma unroll
+    for (int ch = 0; ch < C::D / 32; ++ch) tmem_ld_x32(tO + ch * 32, o[ch]);
+    if constexpr (C::kLOnes) tmem_ld_x16(tO + C::D, ol);
+    tmem_ld_wait();
+    const uint64_t alpha2 = pack_f32x2(alpha, alpha);
+#pragma unroll
+    for (int ch = 0; ch < C::D / 32; ++ch) {
+      reg_fence_x32(o[ch]);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float a, b;
+        unpack_f32x2(fmul2(pack_f32x2(__uint_as_float(o[ch][i]), __uint_as_float(o[ch][i + 1])), alpha2), a, b);
+        o[ch][i] = __float_as_uint(a);
+        o[ch][i + 1] = __float_as_uint(b);
+      }
+      tmem_st_x32(tO + ch * 32, o[ch]);
+    }
+    if constexpr (C::kLOnes) {
+      reg_fence_x16(ol);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ol[i] = __float_as_uint(__uint_as_float(ol[i]) * alpha);
+      tmem_st_x16(tO + C::D, ol);
+    }
+  }
+  tmem_st_wait();
+  tc_fence_before_sync();
+  mbar_arrive(pbar);
+  m_run = m_use;}
+
+template <class C, bool kCausal, bool kMod, bool kWin>
+__global__ void __launch_bounds__(C::kThreads, 1)
+  fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                 const FwdParams p) {
+  using namespace ptx;
+extern __shared__ uint8_t smem_raw[];
+const uint32_t raw = smem_u32(smem_raw);
+const uint32_t base = (raw + 1023u) & ~1023u;
+uint8_t* gbase = smem_raw + (base - raw);
+volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(gbase + C::kOffMisc);
+// misc[0] TMEM base address, misc[1] abort flag, misc[2] status at CTA start
+
+const int warp = static_cast<int>(threadIdx.x) / 32;
+const int lane = static_cast<int>(threadIdx.x) % 32;
+auto bar = [&](int i) -> uint32_t { return base + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+
+const int split = static_cast<int>(blockIdx.x) % p.num_splits;
+const int kb = split * p.tiles_per_split;  // first key tile of this CTA's split
+const Unit unit = unit_of_block(p, kCausal, static_cast<int>(blockIdx.x) / p.num_splits);
+const int bh = unit.bh;
+// key/value head read by this query head (grouped-query attention, "From
+// FlashAttention to FlashAttention 2", Layer 8: h_kv = h / (H / H_kv))
+const int bh_kv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
+// Query tile t visits key tiles [kt0[t], kt0[t] + nkv[t]); the CTA streams key
+// tiles ks, ks + 1, ..., ks + n_max - 1 and tile t uses stream positions
+// [jb[t], jb[t] + nkv[t]).  Without a window every tile starts at the split's
+// first key tile, so jb is 0.
+int row0[C::kQTiles], kt0[C::kQTiles], nkv[C::kQTiles], jb[C::kQTiles];
+int ks = kb, n_max = 0;
+#pragma unroll
+for (int t = 0; t < C::kQTiles; ++t) {
+  row0[t] = tile_first_row(p, unit, t, C::kQTiles);
+  const KvSpan sp = kv_span<kWin, C::BN>(row0[t], p, kCausal, split);
+  kt0[t] = sp.first;
+  nkv[t] = sp.count;
+  jb[t] = 0;
+  n_max = max(n_max, nkv[t]);
+}
+if constexpr (kWin) {
+  int lo = 0x7fffffff, hi = 0;
+#pragma unroll
+  for (int t = 0; t < C::kQTiles; ++t)
+    if (nkv[t] > 0) {
+      lo = min(lo, kt0[t]);
+      hi = max(hi, kt0[t] + nkv[t]);
+    }
+  ks = hi > 0 ? lo : 0;
+  n_max = hi > 0 ? hi - lo : 0;
+#pragma unroll
+  for (int t = 0; t < C::kQTiles; ++t) jb[t] = kt0[t] - ks;
+}
+
+// ------------------------------------------------------------ set-up
+if (threadIdx.x == 0) {
+  misc[1] = 0u;
+  misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
+  for (int t = 0; t < C::kQTiles; ++t) {
+    mbar_init(bar(C::kBarQ + t), 1);
+    mbar_init(bar(C::kBarSFull + t), 1);
+    mbar_init(bar(C::kBarPFull + t), 128 * C::kHalves);
+    if (C::kHalves == 2) mbar_init(bar(C::kBarX + t), 256);
+    mbar_init(bar(C::kBarOFull + t), 1);
+  }
+  for (int s = 0; s < C::kStages; ++s) {
+    mbar_init(bar(C::kBarKFull + s), 1);
+    mbar_init(bar(C::kBarFree + s), 1);
+    mbar_init(bar(C::kBarVFull + s), 1);
+  }
+  mbar_init(bar(C::kBarMmaDone), 1);
+  fence_mbar_init();
+}
+if (warp == C::kTmaWarp && lane == 0) {
+  prefetch_tensormap(&tmQ);
+  prefetch_tensormap(&tmK);
+  prefetch_tensormap(&tmV);
+  prefetch_tensormap(&tmO);
+}
+if (warp == C::kMmaWarp) {
+  tmem_alloc(base + C::kOffMisc, C::kTmemCols);
+  tmem_relinquish_alloc_permit();
+}
+if constexpr (C::kLOnes) {
+  // the ones block of every V stage (TMA writes only the blocks before it)
+  const uint32_t one2 = C::kBF16 ? 0x3F803F80u : 0x3F800000u;
+  for (int i = static_cast<int>(threadIdx.x); i < C::kStages * (C::kKVBlockBytes / 16); i += C::kThreads) {
+    const int st = i / (C::kKVBlockBytes / 16), o = i % (C::kKVBlockBytes / 16);
+    st_shared_v4(base + C::kOffV + st * C::kVTileBytes + C::kColBlocks * C::kKVBlockBytes + o * 16, one2, one2,
+                 one2, one2);
+  }
+  fence_proxy_async_smem();  // visible to the tensor core (async proxy)
+}
+tc_fence_before_sync();
+__syncthreads();
+tc_fence_after_sync();
+const uint32_t tmem = misc[0];
+const bool skip = misc[2] != 0u;  // an earlier launch failed: do nothing
+const WaitCtx wctx{misc + 1, p.status};
+
+if (!skip && warp == C::kTmaWarp) {
+  // ---------------------------------------------------------- TMA producer
+  if (lane == 0) {
+    const uint64_t pol_kv = l2_policy_evict_last();
+    const uint64_t pol_q = l2_policy_evict_first();
+#pragma unroll
+    for (int t = 0; t < C::kQTiles; ++t) {
+      if (nkv[t] == 0) continue;
+      mbar_arrive_expect_tx(bar(C::kBarQ + t), C::kTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ,
+                         bar(C::kBarQ + t), cb * C::kSwElems, row0[t], tile_head(p, unit, t), pol_q);
+    }
+    int issued = 0;  // K/V tiles whose loads were issued
+    for (int j = 0; j < n_max; ++j) {
+      const int s = j % C::kStages;
+      const uint32_t use = static_cast<uint32_t>(j / C::kStages);
+      // K_j replaces K_{j-S}, free after MMA round j-S; V_j replaces V_{j-S}, free
+      // after round j-S+1 (which ran P V on it).  One barrier per round.
+      if (use > 0 && !wait_bounded(bar(C::kBarFree + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaK))
+        break;
+      mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kKTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d_hint(base + C::kOffK + s * C::kKTileBytes + cb * C::kKVBlockBytes, &tmK,
+                         bar(C::kBarKFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
+      if (use > 0 && !wait_bounded(bar(C::kBarFree + (j - C::kStages + 1) % C::kStages),
+                                   static_cast<uint32_t>((j - C::kStages + 1) / C::kStages) & 1u, wctx,
+                                   kStatusTimeoutTmaV)) {
+        issued = -(j + 1);  // K_j issued, V_j not
+        break;
+      }
+      mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kKTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d_hint(base + C::kOffV + s * C::kVTileBytes + cb * C::kKVBlockBytes, &tmV,
+                         bar(C::kBarVFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
+      issued = j + 1;
+    }
+    if (*wctx.abort_flag) {
+      // wind down: every issued copy must land before the CTA's smem is released
+      const int k_done = issued >= 0 ? issued : -issued;
+      const int v_done = issued >= 0 ? issued : -issued - 1;
+      for (int t = 0; t < C::kQTiles; ++t)
+        if (nkv[t] > 0) drain_bounded(bar(C::kBarQ + t), 0);
+      for (int j = max(0, k_done - C::kStages); j < k_done; ++j)
+        drain_bounded(bar(C::kBarKFull + j % C::kStages), (j / C::kStages) & 1);
+      for (int j = max(0, v_done - C::kStages); j < v_done; ++j)
+        drain_bounded(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1);
+    }
+  }
+  __syncwarp();
+} else if (!skip && warp == C::kMmaWarp) {
+  // ---------------------------------------------------------- MMA issuer
+  if (lane == 0) {
+    // Descriptor words of the operand tiles.  The low word holds the start
+    // address >> 4, so a K step or another ring stage is one 32-bit add to it;
+    // fewer instructions between MMAs keep the tensor core's queue fed while
+    // the softmax warps share this warp's scheduler.
+    const uint64_t qk_desc = smem_desc_sw128(base, 16, 1024);
+    const uint32_t qk_lo0 = static_cast<uint32_t>(qk_desc), qk_hi = static_cast<uint32_t>(qk_desc >> 32);
+    const uint64_t v_desc = C::kBF16 ? smem_desc(base + C::kOffV, C::kKVBlockBytes, 1024, kLayoutSw128)
+                                     : smem_desc(base + C::kOffV, C::kKVBlockBytes, 512, kLayoutSw128Atom32);
+    const uint32_t v_lo0 = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
+    bool ok = true;
 #pragma unroll
     for (int t = 0; t < C::kQTiles; ++t)
-      if (nkv[t] > 0) {
-        lo = min(lo, kt0[t]);
-        hi = max(hi, kt0[t] + nkv[t]);
-      }
-    ks = hi > 0 ? lo : 0;
-    n_max = hi > 0 ? hi - lo : 0;
-#pragma unroll
-    for (int t = 0; t < C::kQTiles; ++t) jb[t] = kt0[t] - ks;
-  }
-
-  // ------------------------------------------------------------ set-up
-  if (threadIdx.x == 0) {
-    misc[1] = 0u;
-    misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
-    for (int t = 0; t < C::kQTiles; ++t) {
-      mbar_init(bar(C::kBarQ + t), 1);
-      mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), 128 * C::kHalves);
-      if (C::kHalves == 2) mbar_init(bar(C::kBarX + t), 256);
-      mbar_init(bar(C::kBarOFull + t), 1);
-    }
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(C::kBarKFull + s), 1);
-      mbar_init(bar(C::kBarFree + s), 1);
-      mbar_init(bar(C::kBarVFull + s), 1);
-    }
-    mbar_init(bar(C::kBarMmaDone), 1);
-    fence_mbar_init();
-  }
-  if (warp == C::kTmaWarp && lane == 0) {
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-    prefetch_tensormap(&tmO);
-  }
-  if (warp == C::kMmaWarp) {
-    tmem_alloc(base + C::kOffMisc, C::kTmemCols);
-    tmem_relinquish_alloc_permit();
-  }
-  if constexpr (C::kLOnes) {
-    // the ones block of every V stage (TMA writes only the blocks before it)
-    const uint32_t one2 = C::kBF16 ? 0x3F803F80u : 0x3F800000u;
-    for (int i = static_cast<int>(threadIdx.x); i < C::kStages * (C::kKVBlockBytes / 16); i += C::kThreads) {
-      const int st = i / (C::kKVBlockBytes / 16), o = i % (C::kKVBlockBytes / 16);
-      st_shared_v4(base + C::kOffV + st * C::kVTileBytes + C::kColBlocks * C::kKVBlockBytes + o * 16, one2, one2,
-                   one2, one2);
-    }
-    fence_proxy_async_smem();  // visible to the tensor core (async proxy)
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = misc[0];
-  const bool skip = misc[2] != 0u;  // an earlier launch failed: do nothing
-  const WaitCtx wctx{misc + 1, p.status};
-
-  if (!skip && warp == C::kTmaWarp) {
-    // ---------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      const uint64_t pol_kv = l2_policy_evict_last();
-      const uint64_t pol_q = l2_policy_evict_first();
+      if (ok && nkv[t] > 0) ok = wait_bounded(bar(C::kBarQ + t), 0, wctx, kStatusTimeoutMmaQ);
+    for (int j = 0; ok && j <= n_max; ++j) {
+      const int s = j % C::kStages;
+      bool v_ready = false, k_ready = false;
 #pragma unroll
       for (int t = 0; t < C::kQTiles; ++t) {
-        if (nkv[t] == 0) continue;
-        mbar_arrive_expect_tx(bar(C::kBarQ + t), C::kTileBytes);
-#pragma unroll
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ,
-                           bar(C::kBarQ + t), cb * C::kSwElems, row0[t], tile_head(p, unit, t), pol_q);
-      }
-      int issued = 0;  // K/V tiles whose loads were issued
-      for (int j = 0; j < n_max; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t use = static_cast<uint32_t>(j / C::kStages);
-        // K_j replaces K_{j-S}, free after MMA round j-S; V_j replaces V_{j-S}, free
-        // after round j-S+1 (which ran P V on it).  One barrier per round.
-        if (use > 0 && !wait_bounded(bar(C::kBarFree + s), (use - 1) & 1u, wctx, kStatusTimeoutTmaK))
-          break;
-        mbar_arrive_expect_tx(bar(C::kBarKFull + s), C::kKTileBytes);
-#pragma unroll
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d_hint(base + C::kOffK + s * C::kKTileBytes + cb * C::kKVBlockBytes, &tmK,
-                           bar(C::kBarKFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
-        if (use > 0 && !wait_bounded(bar(C::kBarFree + (j - C::kStages + 1) % C::kStages),
-                                     static_cast<uint32_t>((j - C::kStages + 1) / C::kStages) & 1u, wctx,
-                                     kStatusTimeoutTmaV)) {
-          issued = -(j + 1);  // K_j issued, V_j not
-          break;
-        }
-        mbar_arrive_expect_tx(bar(C::kBarVFull + s), C::kKTileBytes);
-#pragma unroll
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d_hint(base + C::kOffV + s * C::kVTileBytes + cb * C::kKVBlockBytes, &tmV,
-                           bar(C::kBarVFull + s), cb * C::kSwElems, (ks + j) * C::BN, bh_kv, pol_kv);
-        issued = j + 1;
-      }
-      if (*wctx.abort_flag) {
-        // wind down: every issued copy must land before the CTA's smem is released
-        const int k_done = issued >= 0 ? issued : -issued;
-        const int v_done = issued >= 0 ? issued : -issued - 1;
-        for (int t = 0; t < C::kQTiles; ++t)
-          if (nkv[t] > 0) drain_bounded(bar(C::kBarQ + t), 0);
-        for (int j = max(0, k_done - C::kStages); j < k_done; ++j)
-          drain_bounded(bar(C::kBarKFull + j % C::kStages), (j / C::kStages) & 1);
-        for (int j = max(0, v_done - C::kStages); j < v_done; ++j)
-          drain_bounded(bar(C::kBarVFull + j % C::kStages), (j / C::kStages) & 1);
-      }
-    }
-    __syncwarp();
-  } else if (!skip && warp == C::kMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      // Descriptor words of the operand tiles.  The low word holds the start
-      // address >> 4, so a K step or another ring stage is one 32-bit add to it;
-      // fewer instructions between MMAs keep the tensor core's queue fed while
-      // the softmax warps share this warp's scheduler.
-      const uint64_t qk_desc = smem_desc_sw128(base, 16, 1024);
-      const uint32_t qk_lo0 = static_cast<uint32_t>(qk_desc), qk_hi = static_cast<uint32_t>(qk_desc >> 32);
-      const uint64_t v_desc = C::kBF16 ? smem_desc(base + C::kOffV, C::kKVBlockBytes, 1024, kLayoutSw128)
-                                       : smem_desc(base + C::kOffV, C::kKVBlockBytes, 512, kLayoutSw128Atom32);
-      const uint32_t v_lo0 = static_cast<uint32_t>(v_desc), v_hi = static_cast<uint32_t>(v_desc >> 32);
-      bool ok = true;
-#pragma unroll
-      for (int t = 0; t < C::kQTiles; ++t)
-        if (ok && nkv[t] > 0) ok = wait_bounded(bar(C::kBarQ + t), 0, wctx, kStatusTimeoutMmaQ);
-      for (int j = 0; ok && j <= n_max; ++j) {
-        const int s = j % C::kStages;
-        bool v_ready = false, k_ready = false;
-#pragma unroll
-        for (int t = 0; t < C::kQTiles; ++t) {
-          if ((kWin ? j - 1 >= jb[t] : j >= 1) && j - 1 < jb[t] + nkv[t]) {
-            // O_t += P_t V_{j-1}
-            const int jp = j - 1;
-            const int sv = jp % C::kStages;
-            // V first: it has normally landed long ago, and checking it while P is
-            // still being written keeps that check off the path from P to the MMAs
-            if (!v_ready) {
-              ok = wait_bounded(bar(C::kBarVFull + sv), (jp / C::kStages) & 1, wctx, kStatusTimeoutMmaV);
-              if (!ok) break;
-              v_ready = true;
-            }
-            ok = wait_bounded(bar(C::kBarPFull + t), (kWin ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
+        if ((kWin ? j - 1 >= jb[t] : j >= 1) && j - 1 < jb[t] + nkv[t]) {
+          // O_t += P_t V_{j-1}
+          const int jp = j - 1;
+          const int sv = jp % C::kStages;
+          // V first: it has normally landed long ago, and checking it while P is
+          // still being written keeps that check off the path from P to the MMAs
+          if (!v_ready) {
+            ok = wait_bounded(bar(C::kBarVFull + sv), (jp / C::kStages) & 1, wctx, kStatusTimeoutMmaV);
             if (!ok) break;
-            tc_fence_after_sync();
-            const uint32_t v_lo = v_lo0 + static_cast<uint32_t>(sv) * (C::kVTileBytes >> 4);
-            const int jp0 = kWin ? jb[t] : 0;  // first P V of this tile overwrites O
-#pragma unroll
-            for (int kk = 0; kk < C::kStepsPV; ++kk) {
-              // B = V rows [kk*kMmaK, +kMmaK), all D columns, MN-major
-              const uint64_t bdesc = desc_from_words(v_lo + (kk * C::kMmaK * 128 >> 4), v_hi);
-              const uint32_t a_tmem = tmem + C::kColS(t) + kk * 8;
-              if constexpr (C::kBF16)
-                mma_f16_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
-              else
-                mma_tf32_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
-            }
-            // O_t is read by the epilogue after its last P V; a rescale on the way
-            // needs no barrier of its own (it follows S_{jp+1}, issued after this)
-            if (jp == jb[t] + nkv[t] - 1) tc_commit(bar(C::kBarOFull + t));
+            v_ready = true;
           }
-          if ((kWin ? j >= jb[t] : true) && j < jb[t] + nkv[t]) {
-            // S_t = Q_t K_j^T
-            if (!k_ready) {
-              ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
-              if (!ok) break;
-              k_ready = true;
-              tc_fence_after_sync();
-            }
-            const uint32_t q_lo = qk_lo0 + ((C::kOffQ + t * C::kTileBytes) >> 4);
-            const uint32_t k_lo = qk_lo0 + ((C::kOffK >> 4) + static_cast<uint32_t>(s) * (C::kKTileBytes >> 4));
-#pragma unroll
-            for (int kk = 0; kk < C::kStepsS; ++kk) {
-              const uint32_t off = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
-              const uint32_t koff = ((kk / 4) * C::kKVBlockBytes + (kk % 4) * 32) >> 4;
-              const uint64_t adesc = desc_from_words(q_lo + off, qk_hi);
-              const uint64_t bdesc = desc_from_words(k_lo + koff, qk_hi);
-              if constexpr (C::kBF16)
-                mma_f16_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
-              else
-                mma_tf32_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(bar(C::kBarSFull + t));
-          }
-        }
-        if (!ok) break;
-        if constexpr (kWin) {
-          // a ring slot is handed back only after its copy landed, even if no
-          // query tile of this CTA read it
-          if (j >= 1 && !v_ready)
-            ok = wait_bounded(bar(C::kBarVFull + (j - 1) % C::kStages), ((j - 1) / C::kStages) & 1, wctx,
-                              kStatusTimeoutMmaV);
-          if (ok && j < n_max && !k_ready)
-            ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
+          ok = wait_bounded(bar(C::kBarPFull + t), (kWin ? jp - jb[t] : jp) & 1, wctx, kStatusTimeoutMmaP);
           if (!ok) break;
-        }
-        // Round j's commit frees K_j (read by this round's S GEMMs) and V_{j-1}
-        // (read by its P V GEMMs); the loader waits for round i - kStages before
-        // loading K_i and for round i - kStages + 1 before loading V_i.
-        if (j < n_max) tc_commit(bar(C::kBarFree + s));
-      }
-      // every MMA issued above must finish before TMEM is released
-      tc_commit(bar(C::kBarMmaDone));
-      drain_bounded(bar(C::kBarMmaDone), 0);
-    }
-    __syncwarp();
-  } else if (!skip && warp < C::kSoftmaxWarps && C::kHalves == 2) {
-    softmax_halves<C, kCausal, kMod, kWin>(p, tmO, unit, split, kb, base, tmem, warp, lane, wctx);
-  } else if (!skip && warp < C::kSoftmaxWarps) {
-    // ---------------------------------------------------------- softmax warpgroups
-    const int t = warp / 4;
-    const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
-    const int tile_row0 = tile_first_row(p, unit, t, C::kQTiles);
-    const int bh_t = tile_head(p, unit, t);
-    const int row = tile_row0 + r;
-    const KvSpan span = kv_span<kWin, C::BN>(tile_row0, p, kCausal, split);
-    const int n_t = span.count;
-    const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + C::kColS(t);
-    const uint32_t tO = tmem + lane_addr + C::kColO(t);
-    // The exponent step computes s * sl2 - base.  With a softcap the kMod path
-    // turns S into log2 units first (sl2 = 1); otherwise S stays in raw q.k units
-    // and the ALiBi penalty is applied in those units (slope / scale).
-    const bool capped = kMod && p.cap_in > 0.f;
-    const float sl2 = capped ? 1.0f : p.scale_log2;
-    float slope_s = 0.f;  // ALiBi slope of this head, in the units S is held in
-    if constexpr (kMod) {
-      if (p.alibi != nullptr) {
-        const float a = p.alibi[(bh_t / p.H) * p.alibi_bstride + bh_t % p.H];
-        slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
-      }
-    }
-    const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
-    float m_run = -INFINITY;  // exponent base in use: a running max of scale*log2e*s
-    float l_run = 0.f;        // running sum of the rounded exp2(s*sl2 - m_run)
-    bool ok = n_t > 0;
-
-    for (int j = 0; ok && j < n_t; ++j) {
-      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + t), j & 1, wctx, kStatusTimeoutSoftmaxS));
-      if (!ok) break;
-      tc_fence_after_sync();
-      // the whole S row of this thread: every TMEM load in flight, one wait (32
-      // columns per load; a 112-key row ends with a 16-column load)
-      constexpr int kLd = (C::BN + 31) / 32;
-      uint32_t v[kLd][32];
-#pragma unroll
-      for (int ch = 0; ch < C::BN / 32; ++ch) tmem_ld_x32(tS + ch * 32, v[ch]);
-      if constexpr (C::BN % 32 == 16)
-        tmem_ld_x16(tS + (C::BN / 32) * 32, *reinterpret_cast<uint32_t(*)[16]>(&v[kLd - 1][0]));
-      tmem_ld_wait();
-#pragma unroll
-      for (int ch = 0; ch < C::BN / 32; ++ch) reg_fence_x32(v[ch]);
-      if constexpr (C::BN % 32 == 16) reg_fence_x16(*reinterpret_cast<uint32_t(*)[16]>(&v[kLd - 1][0]));
-      static_assert(C::BN % 32 == 0 || C::BN % 32 == 16, "S rows load in 32- and 16-column pieces");
-      float s[C::BN];
-#pragma unroll
-      for (int c = 0; c < C::BN; ++c) s[c] = __uint_as_float(v[c / 32][c % 32]);
-      const int key0 = ((kWin ? span.first : kb) + j) * C::BN;
-      if constexpr (kMod) {
-        // score modifiers: softcap (into log2 units), then the ALiBi distance penalty
-        if (capped) {
-#pragma unroll
-          for (int c = 0; c < C::BN; ++c) s[c] = p.cap_out * tanh_mufu(s[c] * p.cap_in);
-        }
-        if (slope_s != 0.f) {
-          const float d0 = static_cast<float>(key0 - row);
-#pragma unroll
-          for (int c = 0; c < C::BN; ++c) s[c] = fmaf(-slope_s, fabsf(d0 + static_cast<float>(c)), s[c]);
-        }
-      }
-      if constexpr (kWin) {
-        // window mask, on tiles that cross N or either window edge of some row
-        const bool boundary = (key0 + C::BN > p.N) || (key0 + C::BN - 1 > tile_row0 + p.win_right) ||
-                              (key0 < tile_row0 + C::BM - 1 - p.win_left);
-        if (boundary) {
-          const int hi = min(p.N - 1, row + p.win_right) - key0;
-          const int lo = row - p.win_left - key0;
-#pragma unroll
-          for (int c = 0; c < C::BN; ++c) s[c] = (c >= lo && c <= hi) ? s[c] : -INFINITY;
-        }
-      } else {
-        // mask keys past N and, when causal, keys after this row (boundary tiles only)
-        const bool boundary = (key0 + C::BN > p.N) || (kCausal && key0 + C::BN - 1 > tile_row0);
-        if (boundary) {
-          int lim = p.N - 1 - key0;
-          if (kCausal) lim = min(lim, row - key0);
-#pragma unroll
-          for (int c = 0; c < C::BN; ++c) s[c] = (c <= lim) ? s[c] : -INFINITY;
-        }
-      }
-      // row max: four independent chains of 3-input max over s[4..BN-5], then the
-      // last four columns
-      float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-      for (int c = 4; c + 8 <= C::BN; c += 8) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) mx[q] = fmax3(mx[q], s[c + q], s[c + 4 + q]);
-      }
-      static_assert(C::BN % 8 == 0, "the max chains cover s[0..3], pairs of 4, then s[BN-4..BN-1]");
-      static_assert(C::BN % 64 == 0 || C::BN % 64 == 48, "P is stored in pieces of 64 keys and one of 48");
-#pragma unroll
-      for (int q = 0; q < 4; ++q) mx[q] = fmaxf(mx[q], s[C::BN - 4 + q]);
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-      const float m_new = fmaxf(m_run, m_tile);
-      // Move the exponent base only when the max grew by more than kBaseLagLog2:
-      // the result is exact for any base, and skipping the rescale keeps O in TMEM
-      // untouched on most tiles.  (-inf) - (-inf) is NaN, so an empty row stays put.
-      const bool rescale = (m_new - m_run) > kBaseLagLog2;
-      const float m_use = rescale ? m_new : m_run;
-      const float alpha = rescale ? ex2_approx(m_run - m_new) : 1.0f;
-      const float neg_base = (m_use == -INFINITY) ? 0.f : -m_use;
-      const uint64_t nb2 = pack_f32x2(neg_base, neg_base);
-      // P = exp2(s*sl2 - base), rounded to the P.V operand type.  l sums the
-      // rounded values, so O = sum(P v) / sum(P) is an exact convex combination
-      // of V rows with the weights the tensor core actually used.
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // packed pairs of partial sums
-#pragma unroll
-      for (int h = 0; h < (C::BN + 63) / 64; ++h) {  // pieces of 64 keys (the last of a 112-key row: 48)
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = h * 64 + 2 * i;
-          if (c >= C::BN) break;
-          float x0, x1;
-          unpack_f32x2(ffma2(pack_f32x2(s[c], s[c + 1]), sl2x2, nb2), x0, x1);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if constexpr (C::kBF16) {
-            const uint32_t w = pack_bf16x2(p0, p1);
-            pk[i] = w;
-            if constexpr (!C::kLOnes)
-              acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(__uint_as_float(w << 16),
-                                                        __uint_as_float(w & 0xffff0000u)));
-          } else if constexpr (C::kLOnes) {
-            // fp32 P goes to TMEM as it is: the tensor core reads it as TF32 for the
-            // P V product and for the ones columns alike, so l is the sum of exactly
-            // the weights the product used (an explicit rounding measured 16% slower)
-            s[c] = p0;
-            s[c + 1] = p1;
-          } else {
-            const uint32_t r0 = round_tf32(p0), r1 = round_tf32(p1);
-            s[c] = __uint_as_float(r0);
-            s[c + 1] = __uint_as_float(r1);
-            acc[i % 4] = fadd2(acc[i % 4], pack_f32x2(s[c], s[c + 1]));
-          }
-        }
-        if constexpr (C::kBF16) {
-          if (C::BN - h * 64 >= 64) {
-            tmem_st_x32(tS + h * 32, pk);  // 64 keys -> 32 columns of bf16x2
-          } else {                         // 48 keys -> 24 columns
-            tmem_st_x16(tS + h * 32, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-            tmem_st_x8(tS + h * 32 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&pk[16]));
-          }
-        } else {
-          uint32_t q0[32], q1[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            q0[i] = __float_as_uint(s[h * 64 + i]);
-            q1[i] = __float_as_uint(s[h * 64 + 32 + i]);
-          }
-          tmem_st_x32(tS + h * 64, q0);
-          tmem_st_x32(tS + h * 64 + 32, q1);
-        }
-      }
-      if constexpr (!C::kLOnes) {
-        float a0, a1, a2, a3, a4, a5, a6, a7;
-        unpack_f32x2(acc[0], a0, a1);
-        unpack_f32x2(acc[1], a2, a3);
-        unpack_f32x2(acc[2], a4, a5);
-        unpack_f32x2(acc[3], a6, a7);
-        l_run = l_run * alpha + (((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7)));
-      }
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O_t *= alpha.  P_{j-1} V_{j-1} has landed: the MMA warp issued it before
-        // S_j, and a commit completes only after every earlier MMA.
-        tc_fence_after_sync();
-        // every load of the row in flight at once, one wait
-        uint32_t o[C::D / 32][32];
-        uint32_t ol[16];  // the row sum columns, which scale with O
-#pragma unroll
-        for (int ch = 0; ch < C::D / 32; ++ch) tmem_ld_x32(tO + ch * 32, o[ch]);
-        if constexpr (C::kLOnes) tmem_ld_x16(tO + C::D, ol);
-        tmem_ld_wait();
-        const uint64_t alpha2 = pack_f32x2(alpha, alpha);
-#pragma unroll
-        for (int ch = 0; ch < C::D / 32; ++ch) {
-          reg_fence_x32(o[ch]);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a, b;
-            unpack_f32x2(fmul2(pack_f32x2(__uint_as_float(o[ch][i]), __uint_as_float(o[ch][i + 1])), alpha2), a, b);
-            o[ch][i] = __float_as_uint(a);
-            o[ch][i + 1] = __float_as_uint(b);
-          }
-          tmem_st_x32(tO + ch * 32, o[ch]);
-        }
-        if constexpr (C::kLOnes) {
-          reg_fence_x16(ol);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ol[i] = __float_as_uint(__uint_as_float(ol[i]) * alpha);
-          tmem_st_x16(tO + C::D, ol);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      mbar_arrive(bar(C::kBarPFull + t));
-      m_run = m_use;
-    }
-    // With the ones column the row sum is read from O_t's column D once the last
-    // P V has landed (the epilogue waits for it before using l_run).
-    auto row_sum = [&]() -> float {
-      if constexpr (C::kLOnes) {
-        uint32_t lv[16];
-        tmem_ld_x16(tO + C::D, lv);
-        tmem_ld_wait();
-        reg_fence_x16(lv);
-        return __uint_as_float(lv[0]);
-      } else {
-        return l_run;
-      }
-    };
-
-    // ------------------------------------------------------------ epilogue
-    if (p.num_splits > 1) {
-      // split-KV partial for the rows of this tile: O_s = O/l_s in fp32, L_s (natural
-      // log); a split without visible keys for the tile contributes O_s = 0, L_s = -inf
-      if (tile_row0 < p.M) {
-        if (n_t > 0 && ok)
-          ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx,
-                                                    kStatusTimeoutEpilogue));
-        const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh_t) * p.M + row;
-        float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D);
-        if (n_t > 0 && ok) {
           tc_fence_after_sync();
-          l_run = row_sum();
-          const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+          const uint32_t v_lo = v_lo0 + static_cast<uint32_t>(sv) * (C::kVTileBytes >> 4);
+          const int jp0 = kWin ? jb[t] : 0;  // first P V of this tile overwrites O
 #pragma unroll
-          for (int ch = 0; ch < C::D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld_x32(tO + ch * 32, v);
-            tmem_ld_wait();
-            reg_fence_x32(v);
-            if (row < p.M) {
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                op[ch * 8 + q4] = make_float4(__uint_as_float(v[q4 * 4 + 0]) * inv_l,
-                                              __uint_as_float(v[q4 * 4 + 1]) * inv_l,
-                                              __uint_as_float(v[q4 * 4 + 2]) * inv_l,
-                                              __uint_as_float(v[q4 * 4 + 3]) * inv_l);
-            }
+          for (int kk = 0; kk < C::kStepsPV; ++kk) {
+            // B = V rows [kk*kMmaK, +kMmaK), all D columns, MN-major
+            const uint64_t bdesc = desc_from_words(v_lo + (kk * C::kMmaK * 128 >> 4), v_hi);
+            const uint32_t a_tmem = tmem + C::kColS(t) + kk * 8;
+            if constexpr (C::kBF16)
+              mma_f16_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
+            else
+              mma_tf32_ts(tmem + C::kColO(t), a_tmem, bdesc, C::kIdescPV, (jp > jp0 || kk > 0) ? 1u : 0u);
           }
-          if (row < p.M)
-            p.l_part[prow] = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
-        } else if (n_t == 0 && row < p.M) {
+          // O_t is read by the epilogue after its last P V; a rescale on the way
+          // needs no barrier of its own (it follows S_{jp+1}, issued after this)
+          if (jp == jb[t] + nkv[t] - 1) tc_commit(bar(C::kBarOFull + t));
+        }
+        if ((kWin ? j >= jb[t] : true) && j < jb[t] + nkv[t]) {
+          // S_t = Q_t K_j^T
+          if (!k_ready) {
+            ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
+            if (!ok) break;
+            k_ready = true;
+            tc_fence_after_sync();
+          }
+          const uint32_t q_lo = qk_lo0 + ((C::kOffQ + t * C::kTileBytes) >> 4);
+          const uint32_t k_lo = qk_lo0 + ((C::kOffK >> 4) + static_cast<uint32_t>(s) * (C::kKTileBytes >> 4));
 #pragma unroll
-          for (int q4 = 0; q4 < C::D / 4; ++q4) op[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
-          p.l_part[prow] = -INFINITY;
+          for (int kk = 0; kk < C::kStepsS; ++kk) {
+            const uint32_t off = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
+            const uint32_t koff = ((kk / 4) * C::kKVBlockBytes + (kk % 4) * 32) >> 4;
+            const uint64_t adesc = desc_from_words(q_lo + off, qk_hi);
+            const uint64_t bdesc = desc_from_words(k_lo + koff, qk_hi);
+            if constexpr (C::kBF16)
+              mma_f16_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+            else
+              mma_tf32_ss(tmem + C::kColS(t), adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(C::kBarSFull + t));
         }
       }
-    } else if (n_t > 0 || (kWin && tile_row0 < p.M)) {
-      // (kWin: a window can leave every row of a tile without a visible key; the
-      // tile is then written as O = 0, L = -inf)
-      if (ok)
+      if (!ok) break;
+      if constexpr (kWin) {
+        // a ring slot is handed back only after its copy landed, even if no
+        // query tile of this CTA read it
+        if (j >= 1 && !v_ready)
+          ok = wait_bounded(bar(C::kBarVFull + (j - 1) % C::kStages), ((j - 1) / C::kStages) & 1, wctx,
+                            kStatusTimeoutMmaV);
+        if (ok && j < n_max && !k_ready)
+          ok = wait_bounded(bar(C::kBarKFull + s), (j / C::kStages) & 1, wctx, kStatusTimeoutMmaK);
+        if (!ok) break;
+      }
+      // Round j's commit frees K_j (read by this round's S GEMMs) and V_{j-1}
+      // (read by its P V GEMMs); the loader waits for round i - kStages before
+      // loading K_i and for round i - kStages + 1 before loading V_i.
+      if (j < n_max) tc_commit(bar(C::kBarFree + s));
+    }
+    // every MMA issued above must finish before TMEM is released
+    tc_commit(bar(C::kBarMmaDone));
+    drain_bounded(bar(C::kBarMmaDone), 0);
+  }
+  __syncwarp();
+} else if (!skip && warp < C::kSoftmaxWarps && C::kHalves == 2) {
+  softmax_halves<C, kCausal, kMod, kWin>(p, tmO, unit, split, kb, base, tmem, warp, lane, wctx);
+} else if (!skip && warp < C::kSoftmaxWarps) {
+  // ---------------------------------------------------------- softmax warpgroups
+  const int t = warp / 4;
+  const int r = (warp % 4) * 32 + lane;  // row within the tile = TMEM lane
+  const int tile_row0 = tile_first_row(p, unit, t, C::kQTiles);
+  const int bh_t = tile_head(p, unit, t);
+  const int row = tile_row0 + r;
+  const KvSpan span = kv_span<kWin, C::BN>(tile_row0, p, kCausal, split);
+  const int n_t = span.count;
+  const uint32_t lane_addr = static_cast<uint32_t>((warp % 4) * 32) << 16;
+  const uint32_t tS = tmem + lane_addr + C::kColS(t);
+  const uint32_t tO = tmem + lane_addr + C::kColO(t);
+  // The exponent step computes s * sl2 - base.  With a softcap the kMod path
+  // turns S into log2 units first (sl2 = 1); otherwise S stays in raw q.k units
+  // and the ALiBi penalty is applied in those units (slope / scale).
+  const bool capped = kMod && p.cap_in > 0.f;
+  const float sl2 = capped ? 1.0f : p.scale_log2;
+  float slope_s = 0.f;  // ALiBi slope of this head, in the units S is held in
+  if constexpr (kMod) {
+    if (p.alibi != nullptr) {
+      const float a = p.alibi[(bh_t / p.H) * p.alibi_bstride + bh_t % p.H];
+      slope_s = capped ? a * 1.4426950408889634f : a * (1.4426950408889634f / p.scale_log2);
+    }
+  }
+  const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+  float m_run = -INFINITY;  // exponent base in use: a running max of scale*log2e*s
+  float l_run = 0.f;        // running sum of the rounded exp2(s*sl2 - m_run)
+  bool ok = n_t > 0;
+
+  for (int j = 0; ok && j < n_t; ++j) {
+    ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarSFull + t), j & 1, wctx, kStatusTimeoutSoftmaxS));
+    if (!ok) break;
+    softmax_step<C, kCausal, kMod, kWin>(p, tS, tO, bar(C::kBarPFull + t), ((kWin ? span.first : kb) + j) * C::BN,
+                                         tile_row0, row, capped, slope_s, sl2, sl2x2, j > 0, m_run, l_run);
+  }
+  // With the ones column the row sum is read from O_t's column D once the last
+  // P V has landed (the epilogue waits for it before using l_run).
+  auto row_sum = [&]() -> float {
+    if constexpr (C::kLOnes) {
+      uint32_t lv[16];
+      tmem_ld_x16(tO + C::D, lv);
+      tmem_ld_wait();
+      reg_fence_x16(lv);
+      return __uint_as_float(lv[0]);
+    } else {
+      return l_run;
+    }
+  };
+
+  // ------------------------------------------------------------ epilogue
+  if (p.num_splits > 1) {
+    // split-KV partial for the rows of this tile: O_s = O/l_s in fp32, L_s (natural
+    // log); a split without visible keys for the tile contributes O_s = 0, L_s = -inf
+    if (tile_row0 < p.M) {
+      if (n_t > 0 && ok)
         ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx,
                                                   kStatusTimeoutEpilogue));
-      // Q_t's shared tile is free once the last GEMM of this tile completed: stage O there
-      const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
-      if (kWin && n_t == 0) {
-#pragma unroll
-        for (int cidx = 0; cidx < C::kColBlocks * 8; ++cidx)
-          st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
-        if (row < p.M) p.lse[static_cast<int64_t>(bh_t) * p.M + row] = -INFINITY;
-      } else if (ok) {
+      const int64_t prow = (static_cast<int64_t>(split) * p.BH + bh_t) * p.M + row;
+      float4* op = reinterpret_cast<float4*>(p.o_part + prow * C::D);
+      if (n_t > 0 && ok) {
         tc_fence_after_sync();
         l_run = row_sum();
         const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
@@ -1109,56 +1086,96 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           tmem_ld_x32(tO + ch * 32, v);
           tmem_ld_wait();
           reg_fence_x32(v);
-          if constexpr (C::kBF16) {
+          if (row < p.M) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunks of 8 bf16
-              const int cidx = ch * 4 + q4;
-              const int cb = cidx / 8, c = cidx % 8;
-              const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
-              uint32_t w[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * inv_l,
-                                   __uint_as_float(v[q4 * 8 + 2 * e + 1]) * inv_l);
-              st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-            }
-          } else {
-#pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {  // 16-byte chunks of 4 fp32
-              const int cb = ch, c = q8;
-              const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
-              st_shared_v4(addr, __float_as_uint(__uint_as_float(v[q8 * 4 + 0]) * inv_l),
-                           __float_as_uint(__uint_as_float(v[q8 * 4 + 1]) * inv_l),
-                           __float_as_uint(__uint_as_float(v[q8 * 4 + 2]) * inv_l),
-                           __float_as_uint(__uint_as_float(v[q8 * 4 + 3]) * inv_l));
-            }
+            for (int q4 = 0; q4 < 8; ++q4)
+              op[ch * 8 + q4] = make_float4(__uint_as_float(v[q4 * 4 + 0]) * inv_l,
+                                            __uint_as_float(v[q4 * 4 + 1]) * inv_l,
+                                            __uint_as_float(v[q4 * 4 + 2]) * inv_l,
+                                            __uint_as_float(v[q4 * 4 + 3]) * inv_l);
           }
         }
-        if (row < p.M) {
-          // L = ln(2) * (m + log2 l): the base-2 running state converted to natural log
-          const float L = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
-          p.lse[static_cast<int64_t>(bh_t) * p.M + row] = L;
-        }
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1 + t, 128);
-      if (r == 0 && *wctx.abort_flag == 0u) {
+        if (row < p.M)
+          p.l_part[prow] = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
+      } else if (n_t == 0 && row < p.M) {
 #pragma unroll
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh_t);
-        tma_store_commit();
-        tma_store_wait_read_all();
+        for (int q4 = 0; q4 < C::D / 4; ++q4) op[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.l_part[prow] = -INFINITY;
       }
     }
+  } else if (n_t > 0 || (kWin && tile_row0 < p.M)) {
+    // (kWin: a window can leave every row of a tile without a visible key; the
+    // tile is then written as O = 0, L = -inf)
+    if (ok)
+      ok = __all_sync(0xffffffffu, wait_bounded(bar(C::kBarOFull + t), n_t > 0 ? 0 : 1, wctx,
+                                                kStatusTimeoutEpilogue));
+    // Q_t's shared tile is free once the last GEMM of this tile completed: stage O there
+    const uint32_t stage = base + C::kOffQ + t * C::kTileBytes;
+    if (kWin && n_t == 0) {
+#pragma unroll
+      for (int cidx = 0; cidx < C::kColBlocks * 8; ++cidx)
+        st_shared_v4(stage + (cidx / 8) * C::kBlockBytes + r * 128 + (cidx % 8) * 16, 0u, 0u, 0u, 0u);
+      if (row < p.M) p.lse[static_cast<int64_t>(bh_t) * p.M + row] = -INFINITY;
+    } else if (ok) {
+      tc_fence_after_sync();
+      l_run = row_sum();
+      const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+#pragma unroll
+      for (int ch = 0; ch < C::D / 32; ++ch) {
+        uint32_t v[32];
+        tmem_ld_x32(tO + ch * 32, v);
+        tmem_ld_wait();
+        reg_fence_x32(v);
+        if constexpr (C::kBF16) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunks of 8 bf16
+            const int cidx = ch * 4 + q4;
+            const int cb = cidx / 8, c = cidx % 8;
+            const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * e]) * inv_l,
+                                 __uint_as_float(v[q4 * 8 + 2 * e + 1]) * inv_l);
+            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          }
+        } else {
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {  // 16-byte chunks of 4 fp32
+            const int cb = ch, c = q8;
+            const uint32_t addr = stage + cb * C::kBlockBytes + r * 128 + ((c ^ (r & 7)) << 4);
+            st_shared_v4(addr, __float_as_uint(__uint_as_float(v[q8 * 4 + 0]) * inv_l),
+                         __float_as_uint(__uint_as_float(v[q8 * 4 + 1]) * inv_l),
+                         __float_as_uint(__uint_as_float(v[q8 * 4 + 2]) * inv_l),
+                         __float_as_uint(__uint_as_float(v[q8 * 4 + 3]) * inv_l));
+          }
+        }
+      }
+      if (row < p.M) {
+        // L = ln(2) * (m + log2 l): the base-2 running state converted to natural log
+        const float L = (m_run + lg2_approx(l_run)) * 0.69314718055994530942f;
+        p.lse[static_cast<int64_t>(bh_t) * p.M + row] = L;
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier_sync(1 + t, 128);
+    if (r == 0 && *wctx.abort_flag == 0u) {
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_store_3d(&tmO, stage + cb * C::kBlockBytes, cb * C::kSwElems, tile_row0, bh_t);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
   }
+}
 
-  // ------------------------------------------------------------ teardown
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == C::kMmaWarp) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
+// ------------------------------------------------------------ teardown
+tc_fence_before_sync();
+__syncthreads();
+if (warp == C::kMmaWarp) {
+  tc_fence_after_sync();
+  tmem_dealloc(tmem, C::kTmemCols);
+}
 }
 
 // Host-side launch description shared by the instantiation units.
