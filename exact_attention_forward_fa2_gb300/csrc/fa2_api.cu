@@ -11,6 +11,7 @@
 
 #include "fa2.h"
 #include "fa2_config.h"
+#include "fa2_internal.h"
 #include "fa2_bwd_kernel.cuh"
 #include "fa2_fwd_kernel.cuh"
 
@@ -170,12 +171,10 @@ struct Modifiers {
   int alibi_bstride = 0;
 };
 
-// Shared by every entry point.  num_splits == 1: plain forward; > 1: split-KV
-// partials into `workspace`, then the combine kernel.
-int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int H_kv, int M, int N, int D, float scale, int causal, int dtype, int num_splits,
-                void* workspace, size_t workspace_size, void* stream,
-                const Modifiers& mods = Modifiers()) {
+}  // namespace
+
+int fa2::check_forward_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+                            int H, int H_kv, int M, int N, int D, float scale, int dtype) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_NULL;
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
   if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
@@ -185,6 +184,20 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
   if ((addr(q) | addr(k) | addr(v) | addr(o)) & 15u) return FA2_ERR_ALIGN;
   if (addr(lse) & 3u) return FA2_ERR_ALIGN;
+  return FA2_OK;
+}
+
+namespace {
+
+// Shared by every entry point.  num_splits == 1: plain forward; > 1: split-KV
+// partials into `workspace`, then the combine kernel.
+int run_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int H_kv, int M, int N, int D, float scale, int causal, int dtype, int num_splits,
+                void* workspace, size_t workspace_size, void* stream,
+                const Modifiers& mods = Modifiers()) {
+  const int arg_rc = fa2::check_forward_args(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, dtype);
+  if (arg_rc != FA2_OK) return arg_rc;
+  const auto addr = [](const void* p) { return reinterpret_cast<uintptr_t>(p); };
   if (!(mods.softcap >= 0.f) || std::isinf(mods.softcap)) return FA2_ERR_MODIFIER;
   if (mods.alibi && mods.alibi_bstride != 0 && mods.alibi_bstride != H) return FA2_ERR_MODIFIER;
   if (addr(mods.alibi) & 3u) return FA2_ERR_ALIGN;

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "fa2.h"
+#include "fa2_internal.h"
 
 namespace {
 
@@ -51,8 +52,11 @@ extern "C" int fa2_fwd_splitkv_noalloc(const void* q, const void* k, const void*
                                        float* lse, int B, int H, int H_kv, int M, int N, int D,
                                        float scale, int causal, int dtype, int num_splits,
                                        void* stream) {
+  // the same argument checks as every forward entry, before any CUDA call
+  int rc = fa2::check_forward_args(q, k, v, o, lse, B, H, H_kv, M, N, D, scale, dtype);
+  if (rc != FA2_OK) return rc;
   void* scratch = nullptr;
-  const int rc = scratch_for_current_device(&scratch);
+  rc = scratch_for_current_device(&scratch);
   if (rc != FA2_OK) return rc;
   // fa2_fwd_splitkv lowers num_splits first (auto choice, the 64-slice cap, no
   // empty slice) and then refuses, with FA2_ERR_WORKSPACE, a split whose partials

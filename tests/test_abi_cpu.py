@@ -86,6 +86,20 @@ def test_rejects_bad_arguments(lib, kw, code):
     assert call(lib, **kw) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa2.FA2_ERR_NULL), (dict(lse=None), fa2.FA2_ERR_NULL), (dict(B=0), fa2.FA2_ERR_SHAPE),
+    (dict(D=96), fa2.FA2_ERR_HEADDIM), (dict(dtype=2), fa2.FA2_ERR_DTYPE), (dict(scale=0.0), fa2.FA2_ERR_SCALE),
+    (dict(o=P + 2), fa2.FA2_ERR_ALIGN),
+])
+def test_noalloc_validates_before_any_cuda_call(lib, kw, code):
+    """The allocation-free split-KV entry checks its arguments like fa2_fwd before
+    it looks up its built-in buffer (a CUDA call): same codes, here without a GPU."""
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, M=8, N=8, D=64, scale=0.125, dtype=0)
+    a.update(kw)
+    assert lib.fa2_fwd_splitkv_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], 2, 1, a["M"], a["N"],
+                                       a["D"], a["scale"], 0, a["dtype"], 4, None) == code
+
+
 def call_gqa(lib, H=8, H_kv=2, **kw):
     a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, M=8, N=8, D=64, scale=0.125, causal=0, dtype=0)
     a.update(kw)
