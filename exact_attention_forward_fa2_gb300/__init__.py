@@ -46,6 +46,8 @@ SIGNATURES = {
                      _I, _VP, _SZ, _VP], _I),
     "fa2_bwd": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ,
                  _VP], _I),
+    "fa2_bwd_deterministic": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I,
+                               _VP, _SZ, _VP], _I),
     "fa2_bwd_workspace_bytes": ([_I, _I, _I], _SZ),
     "fa2_bwd_host": ([_VP] * 18 + [_I, _I, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _I, _VP], _I),
     "fa2_fwd_host": ([_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _F, _I, _I,
@@ -381,12 +383,12 @@ def fa2_fwd(q, k, v, o=None, lse=None, scale: float | None = None, causal: bool 
 
 
 def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale: float | None = None,
-            causal: bool = False, workspace=None, stream=None):
-    """Backward pass (C ABI ``fa2_bwd``): gradients (dq, dk, dv) for upstream
-    gradient ``dout``, from the forward's inputs and its outputs ``o`` and
-    ``lse``.  bf16 CUDA tensors; dq like q, dk and dv like k.  The workspace is
-    allocated with torch when not given.  Returns (dq, dk, dv) without
-    synchronising."""
+            causal: bool = False, workspace=None, stream=None, deterministic: bool = False):
+    """Backward pass (C ABI ``fa2_bwd``, or ``fa2_bwd_deterministic`` when
+    ``deterministic``): gradients (dq, dk, dv) for upstream gradient ``dout``,
+    from the forward's inputs and its outputs ``o`` and ``lse``.  bf16 CUDA
+    tensors; dq like q, dk and dv like k.  The workspace is allocated with torch
+    when not given.  Returns (dq, dk, dv) without synchronising."""
     import torch
 
     dtype = _check_qkv(q, k, v)
@@ -409,12 +411,13 @@ def fa2_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scale: float | Non
         need = lib().fa2_bwd_workspace_bytes(B, H, M)
         if workspace is None:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-        rc = lib().fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, M,
-                           N, D, float(scale), 1 if causal else 0, dtype, workspace.data_ptr(),
-                           workspace.numel() * workspace.element_size(), _stream_handle(q, stream))
+        entry = lib().fa2_bwd_deterministic if deterministic else lib().fa2_bwd
+        rc = entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                   dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, M, N, D, float(scale),
+                   1 if causal else 0, dtype, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                   _stream_handle(q, stream))
     if rc != FA2_OK:
-        raise Fa2Error(rc, "fa2_bwd")
+        raise Fa2Error(rc, "fa2_bwd_deterministic" if deterministic else "fa2_bwd")
     return dq, dk, dv
 
 

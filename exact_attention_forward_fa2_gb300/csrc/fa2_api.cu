@@ -291,10 +291,23 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
-// Backward workspace: -L log2(e) and D = rowsum(dO o O), [B*H][M rounded up to 128] fp32 each.
+// Backward workspace: -L log2(e) and D = rowsum(dO o O), [B*H][M rounded up to
+// 128] fp32 each, then the fp32 dQ accumulator of dQ by reduction, [B*H][Mpad][128].
+constexpr int kBwdAccDim = 128;
 size_t bwd_workspace_bytes(int64_t bh, int M) {
   const int64_t mpad = (static_cast<int64_t>(M) + 127) / 128 * 128;
-  return 2 * static_cast<size_t>(bh * mpad) * sizeof(float);
+  return (2 + kBwdAccDim) * static_cast<size_t>(bh * mpad) * sizeof(float);
+}
+
+// Key/value heads per group of the causal dK/dV order when dQ is formed by
+// reduction: the accumulator rows, Q and dO of a group's query heads and its K
+// and V should stay in L2 while the group's CTAs run (two groups overlap).
+int bwd_head_group(int64_t bh_kv, int group, int M, int N, int D) {
+  constexpr double kL2GroupBytes = 32.0 * 1024 * 1024;
+  const int64_t mpad = (static_cast<int64_t>(M) + 127) / 128 * 128;
+  const double per_head = static_cast<double>(group) * (mpad * D * 4.0 + 2.0 * M * D * 2.0) + 2.0 * N * D * 2.0;
+  const int64_t g = static_cast<int64_t>(kL2GroupBytes / per_head);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, bh_kv)));
 }
 
 // Streams and events of the host-buffer pipeline (fa2_fwd_host), created once
@@ -484,10 +497,11 @@ extern "C" size_t fa2_bwd_workspace_bytes(int B, int H, int M) {
   return bwd_workspace_bytes(static_cast<int64_t>(B) * H, M);
 }
 
-extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int M,
-                       int N, int D, float scale, int causal, int dtype, void* workspace,
-                       size_t workspace_size, void* stream) {
+namespace {
+
+int run_backward(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int B, int H, int H_kv, int M, int N, int D, float scale,
+                 int causal, int dtype, void* workspace, size_t workspace_size, void* stream, bool reduce_dq) {
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA2_ERR_NULL;
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return FA2_ERR_SHAPE;
   if (H_kv <= 0 || H % H_kv != 0) return FA2_ERR_SHAPE;
@@ -526,8 +540,12 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
   const int64_t mpad = n_qtiles * 128;
   L.nl2 = static_cast<float*>(workspace);
   L.dlt = L.nl2 + bh * mpad;
+  L.dqacc = (reduce_dq && D == kBwdAccDim) ? L.dlt + bh * mpad : nullptr;
+  L.dq = dq;
   L.params.nl2 = L.nl2;
   L.params.dlt = L.dlt;
+  L.params.dqacc = L.dqacc;
+  L.params.head_group = L.dqacc ? bwd_head_group(bh_kv, H / H_kv, M, N, D) : static_cast<int>(bh_kv);
   L.params.status = st->status;
   L.params.M = M;
   L.params.N = N;
@@ -546,6 +564,24 @@ extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* 
   L.causal = causal ? 1 : 0;
   L.stream = static_cast<cudaStream_t>(stream);
   return fa2::launch_bwd(L, D) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int M,
+                       int N, int D, float scale, int causal, int dtype, void* workspace,
+                       size_t workspace_size, void* stream) {
+  return run_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, H_kv, M, N, D, scale, causal, dtype, workspace,
+                      workspace_size, stream, true);
+}
+
+extern "C" int fa2_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                                     int H, int H_kv, int M, int N, int D, float scale, int causal, int dtype,
+                                     void* workspace, size_t workspace_size, void* stream) {
+  return run_backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, H_kv, M, N, D, scale, causal, dtype, workspace,
+                      workspace_size, stream, false);
 }
 
 extern "C" int fa2_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,

@@ -1,5 +1,7 @@
-// Instantiation and launch of the backward kernels (bf16, head dim 64 and 128):
-// preprocess, then the dK/dV pass, then the dQ pass, all on the caller's stream.
+// Instantiation and launch of the backward kernels (bf16, head dim 64 and 128),
+// all on the caller's stream: preprocess, then either the dK/dV pass and the dQ
+// pass, or (dQ by reduction, head dim 128) the dK/dV/dQ pass and the dQ convert.
+#include <algorithm>
 #include <atomic>
 
 #include "fa2_bwd_kernel.cuh"
@@ -41,16 +43,28 @@ cudaError_t launch_dq(BwdLaunch& L, std::atomic<bool>& attr_done) {
 template <int D>
 cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
   using C = BwdCfg<D, D == 64 ? 8 : 4>;  // deeper ring at D = 64 (keeps one CTA per SM)
-  static std::atomic<bool> attr[64][4] = {};
+  static std::atomic<bool> attr[64][6] = {};
   const int64_t rows_pad = static_cast<int64_t>(L.params.BH) * L.params.Mpad;
   const int64_t need = (rows_pad + 7) / 8;
   const int blocks = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
   bwd_preprocess_kernel<D><<<blocks, 256, 0, L.stream>>>(
       static_cast<const __nv_bfloat16*>(L.o), static_cast<const __nv_bfloat16*>(L.dout), L.lse, L.nl2, L.dlt,
-      L.params.M, L.params.Mpad, rows_pad);
+      L.dqacc, L.params.M, L.params.Mpad, rows_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   std::atomic<bool>* a = attr[dev];
+  if constexpr (D == 128) {
+    if (L.dqacc) {  // dQ by reduction: dK, dV and the dQ accumulator in one pass, then dQ in bf16
+      using CR = BwdCfg<D, 4, true>;
+      e = L.causal ? launch_dkdv<CR, true>(L, a[5]) : launch_dkdv<CR, false>(L, a[4]);
+      if (e != cudaSuccess) return e;
+      const int64_t n8 = static_cast<int64_t>(L.params.BH) * L.params.M * (D / 8);
+      const int64_t cblocks = std::min<int64_t>((n8 + 255) / 256, 16LL * sms);
+      bwd_dq_convert_kernel<D><<<static_cast<unsigned>(cblocks), 256, 0, L.stream>>>(
+          L.dqacc, static_cast<__nv_bfloat16*>(L.dq), L.params.scale, L.params.M, L.params.Mpad, n8);
+      return cudaGetLastError();
+    }
+  }
   e = L.causal ? launch_dkdv<C, true>(L, a[1]) : launch_dkdv<C, false>(L, a[0]);
   if (e != cudaSuccess) return e;
   using CQ = DqCfg<D, D == 64 ? 4 : 3>;  // two query tiles per CTA; K/V ring as deep as fits

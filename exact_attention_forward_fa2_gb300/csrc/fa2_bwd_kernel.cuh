@@ -10,7 +10,9 @@
 //   dV_j  = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
 // The N x N matrices P and dS exist only tile by tile, in TMEM.
 //
-// Three launches:
+// The pages give dQ two ways, "by atomics or by a second pass"; both are here.
+//
+// dQ by a second pass (bitwise reproducible), three launches:
 //   bwd_preprocess    D_i and -L_i log2(e) per query row into a padded workspace
 //                     (rows past M get D = 0 and -L log2(e) = -inf, so their P is 0)
 //   bwd_dkdv_kernel   one CTA per (batch, key/value head, 128-key tile): the pages'
@@ -19,18 +21,28 @@
 //                     in TMEM with four tcgen05 GEMMs per step:
 //                       S^T = K Q^T, dP^T = V dO^T   (keys on TMEM lanes)
 //                       dV += P^T dO, dK += dS^T Q   (P^T, dS^T read from TMEM)
-//   bwd_dq_kernel     one CTA per (batch, head, 128-query tile): the second pass
-//                     the pages allow for dQ instead of atomics.  It streams
-//                     64-row tiles of K and V: S = Q K^T, dP = dO V^T, dQ += dS K.
-// Both GEMM kernels recompute S and dP; dQ needs no atomics, so the result is
-// bitwise reproducible.
+//   bwd_dq_kernel     one CTA per (batch, head, 128-query tile): the second pass.
+//                     It streams 64-row tiles of K and V: S = Q K^T, dP = dO V^T,
+//                     dQ += dS K.
+// Both GEMM kernels recompute S and dP.
+//
+// dQ by reduction (head dim 128; five GEMMs in all instead of seven):
+//   bwd_preprocess    as above, and zeroes an fp32 dQ accumulator [B*H][Mpad][D]
+//   bwd_dkdv_kernel   (kDq) a fifth GEMM per step, dQ^T = K^T dS^T (head dim on
+//                     TMEM lanes, dS^T also written to shared memory), whose
+//                     columns four more warps read out and add into the
+//                     accumulator with fp32 reductions at L2.  The order of the
+//                     adds varies from run to run, so dQ is not bitwise
+//                     reproducible.
+//   bwd_dq_convert    dQ = scale * accumulator, rounded to bf16.
 //
 // Warp roles per CTA: warps 0-3 compute P and dS (thread r owns TMEM lane r),
-// warp 4 issues every tcgen05.mma from one thread, warp 5 issues the TMA copies.
-// TMEM: two stages of {S or S^T: 64 columns, dP or dP^T: 64 columns} so the
-// tensor core computes step t+1 while the CUDA cores work on step t, then the
-// fp32 accumulators (dV and dK, or dQ).  Every mbarrier wait is bounded in time
-// and winds the CTA down like the forward kernel.
+// warp 4 issues every tcgen05.mma from one thread, warp 5 issues the TMA copies,
+// warps 6-9 (kDq) read dQ^T out of TMEM.  TMEM: two stages of {S or S^T: 64
+// columns, dP or dP^T: 64 columns} so the tensor core computes step t+1 while
+// the CUDA cores work on step t, then the fp32 accumulators (dV and dK, or dQ).
+// Every mbarrier wait is bounded in time and winds the CTA down like the
+// forward kernel.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,8 +54,10 @@ namespace fa2 {
 struct BwdParams {
   const float* nl2;   // [BH][Mpad]: -L * log2(e); rows >= M: -inf
   const float* dlt;   // [BH][Mpad]: rowsum(dO o O); rows >= M: 0
+  float* dqacc;       // [BH][Mpad][D] fp32 dQ accumulator (dQ by reduction), else null
   int* status;        // sticky device status word
   int M, N, Mpad;     // Mpad = M rounded up to 128
+  int head_group;     // causal dK/dV order: key/value heads per group (longest tile first within a group)
   int H, group;       // query heads per batch entry; query heads per key/value head
   int BH, BHkv;       // B * H, B * H_kv
   int n_ktiles;       // ceil(N / 128): key tiles per key/value head
@@ -58,18 +72,33 @@ enum : int {
   kStatusBwdTimeoutMmaP = 22,
   kStatusBwdTimeoutSoftmax = 23,
   kStatusBwdTimeoutEpilogue = 24,
+  kStatusBwdTimeoutDrain = 25,
+  kStatusBwdTimeoutMmaDrain = 26,
 };
+
+// Instruction descriptor of the dQ^T = K^T dS^T product: bf16, fp32 accumulate,
+// both operands MN-major (bits 15 and 16; the other fields as make_idesc).
+__host__ __device__ constexpr uint32_t idesc_mn_mn(int m, int n) {
+  return ptx::make_idesc(true, true, m, n) | (1u << 15);
+}
+
+// fp32 add into global memory, performed at L2 (no value returned).
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
 
 // ------------------------------------------------------------------ preprocess
 // One warp per query row: D_i = sum_d dO[i,d] O[i,d] in fp32 from bf16, and
 // -L_i log2(e), the exponent offset of P = exp2(s scale log2(e) - L_i log2(e)).
 // Rows in [M, Mpad) of every head get D = 0 and -inf.
+// With dQ by reduction it also zeroes the row's D accumulator entries.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
                                                              const float* __restrict__ lse,
                                                              float* __restrict__ nl2,
-                                                             float* __restrict__ dlt, int M, int Mpad,
+                                                             float* __restrict__ dlt,
+                                                             float* __restrict__ dqacc, int M, int Mpad,
                                                              int64_t rows_pad) {
   constexpr int kPer = D / 32;
   const int lane = static_cast<int>(threadIdx.x) % 32;
@@ -95,14 +124,45 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       dlt[r] = acc;
       nl2[r] = i < M ? lse[bh * M + i] * -1.4426950408889634f : -INFINITY;
     }
+    if constexpr (kPer % 4 == 0) {
+      if (dqacc) {
+#pragma unroll
+      for (int e = 0; e < kPer; e += 4)
+          *reinterpret_cast<float4*>(dqacc + r * D + lane * kPer + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+}
+
+// dQ[bh][i] = scale * accumulator[bh][i] rounded to bf16, for rows i < M; eight
+// elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dqacc,
+                                                             __nv_bfloat16* __restrict__ dq, float scale,
+                                                             int M, int Mpad, int64_t n8) {
+  for (int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < n8;
+       x += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = x / (D / 8);  // bh * M + i
+    const int c8 = static_cast<int>(x % (D / 8)) * 8;
+    const int64_t bh = row / M;
+    const float* src = dqacc + (bh * Mpad + (row - bh * M)) * D + c8;
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 b = *reinterpret_cast<const float4*>(src + 4);
+    uint4 w;
+    w.x = ptx::pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = ptx::pack_bf16x2(a.z * scale, a.w * scale);
+    w.z = ptx::pack_bf16x2(b.x * scale, b.y * scale);
+    w.w = ptx::pack_bf16x2(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + row * D + c8) = w;
   }
 }
 
 // ------------------------------------------------------------------ shared configuration
-template <int D_, int kStages_>
+template <int D_, int kStages_, bool kDq_ = false>
 struct BwdCfg {
   static constexpr int D = D_;
   static constexpr int kStages = kStages_;  // depth of the ring of streamed tiles
+  static constexpr bool kDq = kDq_;         // dK/dV kernel also forms dQ (by reduction)
   static constexpr int BF = 128;            // rows of the fixed tile (keys or queries)
   static constexpr int BS = 64;             // rows of a streamed tile per step
   static constexpr int kColBlocks = D / 64;  // 128-byte column blocks of a bf16 row
@@ -112,20 +172,27 @@ struct BwdCfg {
   static constexpr int kStrTile = kColBlocks * kStrBlock;
   static constexpr int kMmaK = 16;  // bf16 elements per MMA K step (32 bytes)
   static constexpr int kStepsD = D / kMmaK;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = kDq ? 320 : 192;
   static constexpr int kMmaWarp = 4;
   static constexpr int kTmaWarp = 5;
+  static constexpr int kDrainWarp0 = 6;  // kDq: warps 6-9 (one per TMEM lane quarter)
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: stage s holds S (or S^T) at [128 s, +64) and dP (or dP^T) at
-  // [128 s + 64, +64); P and dS overwrite them as packed bf16 (32 columns each)
+  // [128 s + 64, +64); P and dS overwrite them as packed bf16 (32 columns each):
+  // P over the first half of S, dS over the first half of dP, or with kDq over
+  // the second half of S, so that the step's dQ^T (64 fp32 columns, head dim on
+  // the lanes) accumulates in the dP columns
   __host__ __device__ static constexpr int kColS(int s) { return 128 * s; }
   __host__ __device__ static constexpr int kColDP(int s) { return 128 * s + 64; }
+  __host__ __device__ static constexpr int kColDS(int s) { return kDq ? 128 * s + 32 : 128 * s + 64; }
   static constexpr int kColAcc0 = 256;      // dV (dK/dV kernel) or dQ (dQ kernel)
   static constexpr int kColAcc1 = 256 + D;  // dK (dK/dV kernel)
   static constexpr uint32_t kIdescS = ptx::make_idesc(true, false, BF, BS);  // B K-major, N = 64
   static constexpr uint32_t kIdescAcc = ptx::make_idesc(true, true, BF, D);  // B MN-major, N = D
+  static constexpr uint32_t kIdescDq = idesc_mn_mn(D, BS);  // dQ^T: M = D, N = 64 queries, K = keys
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kColAcc1 + D <= 512, "TMEM budget");
+  static_assert(!kDq || D == 128, "dQ^T has the head dim on TMEM lanes: M = D = 128");
 };
 
 // Bounded waits shared by the roles; `ok` turns false on abort or timeout.
@@ -140,15 +207,21 @@ struct DkvLayout {
   static constexpr int kOffRing = kOffV + C::kFixTile;
   // (a stage starts on a 1024-byte boundary, as the 128-byte swizzle requires)
   static constexpr int kStageBytes = (2 * C::kStrTile + 2 * C::BS * 4 + 1023) / 1024 * 1024;
-  static constexpr int kOffBar = kOffRing + C::kStages * kStageBytes;
-  // barriers: KV, full[S], empty[S], sfull[2], pfull[2], done
+  // kDq: dS^T of one step, [128 keys][64 queries] bf16 in 128-byte swizzled rows
+  static constexpr int kOffDS = kOffRing + C::kStages * kStageBytes;
+  static constexpr int kDSBytes = C::kDq ? C::BF * 128 : 0;
+  static constexpr int kOffBar = kOffDS + kDSBytes;
+  // barriers: KV, full[S], empty[S], sfull[2], pfull[2], done, and with kDq
+  // qfull[2] (dQ^T of the step complete) and qdrained[2] (read out of TMEM)
   static constexpr int kBarKV = 0;
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = kBarFull + C::kStages;
   static constexpr int kBarSFull = kBarEmpty + C::kStages;
   static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarDone = kBarPFull + 2;
-  static constexpr int kNumBars = kBarDone + 1;
+  static constexpr int kBarQFull = kBarDone + 1;
+  static constexpr int kBarQDrained = kBarQFull + 2;
+  static constexpr int kNumBars = C::kDq ? kBarQDrained + 2 : kBarDone + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -170,9 +243,15 @@ struct DkvUnit {
 template <bool kCausal>
 __device__ __forceinline__ DkvUnit dkv_unit(const BwdParams& p, int b) {
   DkvUnit u;
-  if (kCausal) {  // smallest key tile first: it has the most query steps
-    u.jt = b / p.BHkv;
-    u.bhkv = b % p.BHkv;
+  if (kCausal) {
+    // groups of head_group key/value heads one after another; within a group the
+    // smallest key tile first (it has the most query steps).  head_group = BHkv
+    // is one group: smallest key tile first over all heads.
+    const int per = p.head_group * p.n_ktiles;
+    const int g = b / per, rem = b - g * per;
+    const int heads = min(p.head_group, p.BHkv - g * p.head_group);
+    u.jt = rem / heads;
+    u.bhkv = g * p.head_group + rem % heads;
   } else {  // tiles of one key/value head adjacent: Q and dO of its heads stay in L2
     u.bhkv = b / p.n_ktiles;
     u.jt = b % p.n_ktiles;
@@ -219,6 +298,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Lay::kBarSFull + s), 1);
       mbar_init(bar(Lay::kBarPFull + s), 128);
+      if constexpr (C::kDq) {
+        mbar_init(bar(Lay::kBarQFull + s), 1);
+        mbar_init(bar(Lay::kBarQDrained + s), 128);
+      }
     }
     mbar_init(bar(Lay::kBarDone), 1);
     fence_mbar_init();
@@ -287,8 +370,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       // with the P/dS warps).
       const uint64_t dk = smem_desc_sw128(base, 16, 1024);
       const uint64_t dm = smem_desc(base, C::kStrBlock, 1024, kLayoutSw128);
+      // kDq: K^T (A, MN-major: the head dim runs along the 128-byte rows of the
+      // K tile's column blocks, kFixBlock apart) and dS^T (B, MN-major: one
+      // 64-query block); both step along the keys by 8-row groups of 1024 bytes
+      const uint64_t df = smem_desc(base, C::kFixBlock, 1024, kLayoutSw128);
       const uint32_t k_lo0 = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
       const uint32_t m_lo0 = static_cast<uint32_t>(dm), m_hi = static_cast<uint32_t>(dm >> 32);
+      const uint32_t f_lo0 = static_cast<uint32_t>(df), f_hi = static_cast<uint32_t>(df >> 32);
       bool ok = FA2_BWD_WAIT(bar(Lay::kBarKV), 0, kStatusBwdTimeoutMmaLoad);
       for (int t = 0; ok && t <= u.steps; ++t) {
         if (t < u.steps) {
@@ -305,6 +393,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const uint32_t so = ((kk / 4) * C::kStrBlock + (kk % 4) * 32) >> 4;
             mma_f16_ss(tmem + C::kColS(ts), desc_from_words(k_lo0 + (Lay::kOffK >> 4) + fo, k_hi),
                        desc_from_words(q_lo + so, k_hi), C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          if constexpr (C::kDq) {
+            // dP^T of this step overwrites the dQ^T of step t - 2: wait until it was read out
+            if (t >= 2) {
+              ok = FA2_BWD_WAIT(bar(Lay::kBarQDrained + ts), ((t - 2) / 2) & 1, kStatusBwdTimeoutMmaDrain);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
           }
 #pragma unroll
           for (int kk = 0; kk < C::kStepsD; ++kk) {
@@ -329,10 +425,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const uint32_t bo = (kk * C::kMmaK * 128) >> 4;
             mma_f16_ts(tmem + C::kColAcc0, tmem + C::kColS(tsp) + kk * 8, desc_from_words(do_lo + bo, m_hi),
                        C::kIdescAcc, (tp > 0 || kk > 0) ? 1u : 0u);
-            mma_f16_ts(tmem + C::kColAcc1, tmem + C::kColDP(tsp) + kk * 8, desc_from_words(q_lo + bo, m_hi),
+            mma_f16_ts(tmem + C::kColAcc1, tmem + C::kColDS(tsp) + kk * 8, desc_from_words(q_lo + bo, m_hi),
                        C::kIdescAcc, (tp > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar(Lay::kBarEmpty + sp));
+          if constexpr (C::kDq) {
+            // dQ^T = K^T dS^T: M = D, N = 64 queries, K = 128 keys, into the dP^T columns
+#pragma unroll
+            for (int kk = 0; kk < C::BF / C::kMmaK; ++kk) {
+              const uint32_t ko = (kk * C::kMmaK * 128) >> 4;
+              mma_f16_ss(tmem + C::kColDP(tsp), desc_from_words(f_lo0 + (Lay::kOffK >> 4) + ko, f_hi),
+                         desc_from_words(f_lo0 + (Lay::kOffDS >> 4) + ko, f_hi), C::kIdescDq, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(bar(Lay::kBarQFull + tsp));
+          }
         }
       }
       tc_commit(bar(Lay::kBarDone));
@@ -417,8 +523,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           dk[c4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
       }
+      if constexpr (C::kDq) {
+        // the dS^T tile in shared memory is free once the previous step's dQ^T is complete
+        if (t >= 1)
+          ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarQFull + (t - 1) % 2), ((t - 1) / 2) & 1,
+                                                    kStatusBwdTimeoutSoftmax));
+        if (!ok) break;
+      }
       tmem_st_x32(tmem + lane_addr + C::kColS(ts), pk);
-      tmem_st_x32(tmem + lane_addr + C::kColDP(ts), dk);
+      tmem_st_x32(tmem + lane_addr + C::kColDS(ts), dk);
+      if constexpr (C::kDq) {
+        // row r of dS^T (64 queries) as eight 16-byte chunks, chunk c at c ^ (r mod 8)
+        const uint32_t row = base + Lay::kOffDS + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(row + ((c ^ (r & 7)) << 4), dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        fence_proxy_async_smem();
+      }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(Lay::kBarPFull + ts));
@@ -469,6 +590,31 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       }
       tma_store_commit();
       tma_store_wait_read_all();
+    }
+  } else if (!skip && C::kDq && warp >= C::kDrainWarp0) {
+    // ---------------------------------------------------------- dQ read-out
+    // thread d owns TMEM lane d (head-dim column d of dQ^T): per step it reads
+    // the 64 query columns and adds them into rows row0 .. row0 + 63 of the
+    // query head's accumulator, one 128-byte row segment per warp instruction
+    const int quarter = warp % 4;
+    const int d = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    for (int t = 0; t < u.steps; ++t) {
+      const int ts = t % 2;
+      if (!__all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarQFull + ts), (t / 2) & 1, kStatusBwdTimeoutDrain)))
+        break;
+      tc_fence_after_sync();
+      uint32_t v[64];
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld_x32(tmem + lane_addr + C::kColDP(ts) + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait();
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      reg_fence_x32(*reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tc_fence_before_sync();
+      mbar_arrive(bar(Lay::kBarQDrained + ts));
+      float* dst = p.dqacc + (static_cast<int64_t>(step_head(t)) * p.Mpad + step_row0(t)) * C::D + d;
+#pragma unroll
+      for (int q = 0; q < C::BS; ++q) red_add_f32(dst + q * C::D, __uint_as_float(v[q]));
     }
   }
 
@@ -837,6 +983,8 @@ struct BwdLaunch {
   const float* lse;
   float* nl2;
   float* dlt;
+  float* dqacc;    // non-null: dQ by reduction (head dim 128)
+  void* dq;        // bf16 dQ, written by the convert kernel when dqacc is set
   int causal;
   cudaStream_t stream;
 };

@@ -202,8 +202,13 @@ int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse
  * recomputing P = exp(scale q.k - L) tile by tile:  D_i = rowsum(dout o o),
  * dS = P (dout v^T - D),  dv = P^T dout,  dk = scale dS^T q,  dq = scale dS k.
  * With grouped-query attention dk and dv of a key/value head sum over the query
- * heads that read it.  dq is computed by a second pass over the keys (no
- * atomics): results are bitwise reproducible.
+ * heads that read it.  The pages form dq "by atomics or by a second pass"; this
+ * entry takes the first way at D = 128: the dk/dv kernel also forms each step's
+ * dS k and adds it into an fp32 accumulator in the workspace with reductions at
+ * L2, then a small kernel scales it and rounds it to bf16.  The order of those
+ * adds varies between runs, so dq may differ in its last bits from run to run
+ * (dk and dv do not).  At D = 64, and in fa2_bwd_deterministic, dq comes from a
+ * second pass over the keys instead, and every output is bitwise reproducible.
  *
  *   q, o, dout, dq  [B,H,M,D] bf16          k, v, dk, dv  [B,H_kv,N,D] bf16
  *   lse             [B,H,M] fp32, as written by the forward for the same inputs
@@ -212,16 +217,29 @@ int fa2_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse
  *   workspace       caller-owned DEVICE buffer, 256-byte aligned, of at least
  *                   fa2_bwd_workspace_bytes(B, H, M) bytes; scratch on return
  * Device pointers, 16-byte aligned (lse 4-byte); dq, dk, dv are fully
- * overwritten, everything else is only read.  Four kernels are launched on
- * `stream`; concurrent calls must not share a workspace.  Errors as fa2_fwd_gqa,
- * plus FA2_ERR_WORKSPACE and FA2_ERR_TOO_LARGE for M or N above 2^30.
+ * overwritten, everything else is only read.  Three kernels (dq by reduction)
+ * or four (second pass) are launched on `stream`; concurrent calls must not
+ * share a workspace.  Errors as fa2_fwd_gqa, plus FA2_ERR_WORKSPACE and
+ * FA2_ERR_TOO_LARGE for M or N above 2^30.
  */
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
             const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int M, int N,
             int D, float scale, int causal, int dtype, void* workspace, size_t workspace_size,
             void* stream);
 
-/* Workspace bytes fa2_bwd needs: 2 * B*H * (M rounded up to 128) * 4 (0 for invalid sizes). */
+/*
+ * fa2_bwd_deterministic -- fa2_bwd with dq always from the second pass over the
+ * keys (the pages' alternative to atomics) at both head dims: dq, dk and dv are
+ * bitwise reproducible.  Same arguments, workspace and errors as fa2_bwd.
+ */
+int fa2_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                          const void* dout, void* dq, void* dk, void* dv, int B, int H, int H_kv, int M,
+                          int N, int D, float scale, int causal, int dtype, void* workspace,
+                          size_t workspace_size, void* stream);
+
+/* Workspace bytes fa2_bwd and fa2_bwd_deterministic need: (2 + 128) * B*H * (M
+ * rounded up to 128) * 4 -- two fp32 vectors per query row and the fp32 dq
+ * accumulator of dq by reduction (0 for invalid sizes). */
 size_t fa2_bwd_workspace_bytes(int B, int H, int M);
 
 /*
@@ -266,8 +284,9 @@ int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, voi
  *   workspace       as fa2_bwd, sized for the whole problem (every slice reuses it)
  *   chunks          slices (<= 0: 4); at most B*H_kv and 32
  * Host buffers should be page-locked.  Other arguments and errors as fa2_bwd and
- * fa2_fwd_host; the result equals fa2_bwd's bitwise (each slice is its own
- * problem with the same kernels).  The pages have no counterpart to this entry.
+ * fa2_fwd_host; each slice is its own problem with fa2_bwd's kernels, so dk and
+ * dv equal fa2_bwd's bitwise and dq (by reduction at D = 128) within its rounding.
+ * The pages have no counterpart to this entry.
  */
 int fa2_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
                  const float* lse_host, const void* dout_host, void* dq_host, void* dk_host, void* dv_host,

@@ -31,7 +31,8 @@ def lib():
 
 
 def test_header_declares_the_api():
-    assert declared_functions() == ["fa2_bwd", "fa2_bwd_host", "fa2_bwd_workspace_bytes", "fa2_device_status", "fa2_fwd",
+    assert declared_functions() == ["fa2_bwd", "fa2_bwd_deterministic", "fa2_bwd_host", "fa2_bwd_workspace_bytes",
+                                    "fa2_device_status", "fa2_fwd",
                                     "fa2_fwd_ext", "fa2_fwd_gqa", "fa2_fwd_host", "fa2_fwd_splitkv",
                                     "fa2_fwd_splitkv_noalloc", "fa2_probe_ex2", "fa2_selftest_wait_timeout",
                                     "fa2_splitkv_num_splits", "fa2_splitkv_workspace_bytes", "fa2_strerror",
@@ -169,18 +170,19 @@ def test_ext_rejects_bad_arguments(lib, kw, code):
     assert call_ext(lib, **kw) == code
 
 
-def call_bwd(lib, ws=P, ws_bytes=1 << 30, **kw):
+def call_bwd(lib, ws=P, ws_bytes=1 << 30, entry="fa2_bwd", **kw):
     a = dict(q=P, k=P, v=P, o=P, lse=P, do=P, dq=P, dk=P, dv=P, B=2, H=4, H_kv=2, M=100, N=300, D=128,
              scale=0.125, causal=1, dtype=0)
     a.update(kw)
-    return lib.fa2_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["B"],
-                       a["H"], a["H_kv"], a["M"], a["N"], a["D"], a["scale"], a["causal"], a["dtype"], ws,
-                       ws_bytes, None)
+    return getattr(lib, entry)(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                               a["B"], a["H"], a["H_kv"], a["M"], a["N"], a["D"], a["scale"], a["causal"],
+                               a["dtype"], ws, ws_bytes, None)
 
 
 def test_bwd_workspace_bytes(lib):
-    assert lib.fa2_bwd_workspace_bytes(2, 3, 100) == 2 * 2 * 3 * 128 * 4
-    assert lib.fa2_bwd_workspace_bytes(1, 1, 129) == 2 * 256 * 4
+    # two fp32 vectors per padded query row, then the fp32 dQ accumulator (128 per row)
+    assert lib.fa2_bwd_workspace_bytes(2, 3, 100) == 130 * 2 * 3 * 128 * 4
+    assert lib.fa2_bwd_workspace_bytes(1, 1, 129) == 130 * 256 * 4
     assert lib.fa2_bwd_workspace_bytes(0, 1, 1) == 0
 
 
@@ -192,8 +194,9 @@ def test_bwd_workspace_bytes(lib):
     (dict(ws=None), fa2.FA2_ERR_WORKSPACE), (dict(ws=P + 128), fa2.FA2_ERR_WORKSPACE),
     (dict(ws_bytes=1024), fa2.FA2_ERR_WORKSPACE), (dict(N=(1 << 30) + 1), fa2.FA2_ERR_TOO_LARGE),
 ])
-def test_bwd_rejects_bad_arguments(lib, kw, code):
-    assert call_bwd(lib, **kw) == code
+@pytest.mark.parametrize("entry", ["fa2_bwd", "fa2_bwd_deterministic"])
+def test_bwd_rejects_bad_arguments(lib, kw, code, entry):
+    assert call_bwd(lib, entry=entry, **kw) == code
 
 
 def call_host(lib, **kw):
