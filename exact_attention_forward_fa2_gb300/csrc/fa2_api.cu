@@ -299,16 +299,6 @@ size_t bwd_workspace_bytes(int64_t bh, int M) {
   return (2 + kBwdAccDim) * static_cast<size_t>(bh * mpad) * sizeof(float);
 }
 
-// Key/value heads per group of the causal dK/dV order when dQ is formed by
-// reduction: the accumulator rows, Q and dO of a group's query heads and its K
-// and V should stay in L2 while the group's CTAs run (two groups overlap).
-int bwd_head_group(int64_t bh_kv, int group, int M, int N, int D) {
-  constexpr double kL2GroupBytes = 32.0 * 1024 * 1024;
-  const int64_t mpad = (static_cast<int64_t>(M) + 127) / 128 * 128;
-  const double per_head = static_cast<double>(group) * (mpad * D * 4.0 + 2.0 * M * D * 2.0) + 2.0 * N * D * 2.0;
-  const int64_t g = static_cast<int64_t>(kL2GroupBytes / per_head);
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(g, bh_kv)));
-}
 
 // Streams and events of the host-buffer pipeline (fa2_fwd_host), created once
 // per device; the whole enqueue sequence of one call holds the mutex.
@@ -545,7 +535,6 @@ int run_backward(const void* q, const void* k, const void* v, const void* o, con
   L.params.nl2 = L.nl2;
   L.params.dlt = L.dlt;
   L.params.dqacc = L.dqacc;
-  L.params.head_group = L.dqacc ? bwd_head_group(bh_kv, H / H_kv, M, N, D) : static_cast<int>(bh_kv);
   L.params.status = st->status;
   L.params.M = M;
   L.params.N = N;

@@ -57,7 +57,6 @@ struct BwdParams {
   float* dqacc;       // [BH][Mpad][D] fp32 dQ accumulator (dQ by reduction), else null
   int* status;        // sticky device status word
   int M, N, Mpad;     // Mpad = M rounded up to 128
-  int head_group;     // causal dK/dV order: key/value heads per group (longest tile first within a group)
   int H, group;       // query heads per batch entry; query heads per key/value head
   int BH, BHkv;       // B * H, B * H_kv
   int n_ktiles;       // ceil(N / 128): key tiles per key/value head
@@ -158,11 +157,12 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
 }
 
 // ------------------------------------------------------------------ shared configuration
-template <int D_, int kStages_, bool kDq_ = false>
+template <int D_, int kStages_, bool kDq_ = false, int kDsBufs_ = 1>
 struct BwdCfg {
   static constexpr int D = D_;
   static constexpr int kStages = kStages_;  // depth of the ring of streamed tiles
   static constexpr bool kDq = kDq_;         // dK/dV kernel also forms dQ (by reduction)
+  static constexpr int kDsBufs = kDsBufs_;  // kDq: dS^T tiles in shared memory (1 or 2)
   static constexpr int BF = 128;            // rows of the fixed tile (keys or queries)
   static constexpr int BS = 64;             // rows of a streamed tile per step
   static constexpr int kColBlocks = D / 64;  // 128-byte column blocks of a bf16 row
@@ -209,7 +209,8 @@ struct DkvLayout {
   static constexpr int kStageBytes = (2 * C::kStrTile + 2 * C::BS * 4 + 1023) / 1024 * 1024;
   // kDq: dS^T of one step, [128 keys][64 queries] bf16 in 128-byte swizzled rows
   static constexpr int kOffDS = kOffRing + C::kStages * kStageBytes;
-  static constexpr int kDSBytes = C::kDq ? C::BF * 128 : 0;
+  static constexpr int kDSTile = C::BF * 128;
+  static constexpr int kDSBytes = C::kDq ? C::kDsBufs * kDSTile : 0;
   static constexpr int kOffBar = kOffDS + kDSBytes;
   // barriers: KV, full[S], empty[S], sfull[2], pfull[2], done, and with kDq
   // qfull[2] (dQ^T of the step complete) and qdrained[2] (read out of TMEM)
@@ -243,15 +244,9 @@ struct DkvUnit {
 template <bool kCausal>
 __device__ __forceinline__ DkvUnit dkv_unit(const BwdParams& p, int b) {
   DkvUnit u;
-  if (kCausal) {
-    // groups of head_group key/value heads one after another; within a group the
-    // smallest key tile first (it has the most query steps).  head_group = BHkv
-    // is one group: smallest key tile first over all heads.
-    const int per = p.head_group * p.n_ktiles;
-    const int g = b / per, rem = b - g * per;
-    const int heads = min(p.head_group, p.BHkv - g * p.head_group);
-    u.jt = rem / heads;
-    u.bhkv = g * p.head_group + rem % heads;
+  if (kCausal) {  // smallest key tile first: it has the most query steps
+    u.jt = b / p.BHkv;
+    u.bhkv = b % p.BHkv;
   } else {  // tiles of one key/value head adjacent: Q and dO of its heads stay in L2
     u.bhkv = b / p.n_ktiles;
     u.jt = b % p.n_ktiles;
@@ -434,8 +429,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < C::BF / C::kMmaK; ++kk) {
               const uint32_t ko = (kk * C::kMmaK * 128) >> 4;
+              const uint32_t dso = (Lay::kOffDS + (tp % C::kDsBufs) * Lay::kDSTile) >> 4;
               mma_f16_ss(tmem + C::kColDP(tsp), desc_from_words(f_lo0 + (Lay::kOffK >> 4) + ko, f_hi),
-                         desc_from_words(f_lo0 + (Lay::kOffDS >> 4) + ko, f_hi), C::kIdescDq, kk > 0 ? 1u : 0u);
+                         desc_from_words(f_lo0 + dso + ko, f_hi), C::kIdescDq, kk > 0 ? 1u : 0u);
             }
             tc_commit(bar(Lay::kBarQFull + tsp));
           }
@@ -523,8 +519,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           dk[c4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
       }
-      if constexpr (C::kDq) {
-        // the dS^T tile in shared memory is free once the previous step's dQ^T is complete
+      if constexpr (C::kDq && C::kDsBufs == 1) {
+        // the dS^T tile in shared memory is free once the previous step's dQ^T is
+        // complete (with two tiles, the one of step t - 2 is: its dQ^T was issued
+        // before this step's S^T, whose completion the wait on sfull saw)
         if (t >= 1)
           ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarQFull + (t - 1) % 2), ((t - 1) / 2) & 1,
                                                     kStatusBwdTimeoutSoftmax));
@@ -534,7 +532,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
       tmem_st_x32(tmem + lane_addr + C::kColDS(ts), dk);
       if constexpr (C::kDq) {
         // row r of dS^T (64 queries) as eight 16-byte chunks, chunk c at c ^ (r mod 8)
-        const uint32_t row = base + Lay::kOffDS + r * 128;
+        const uint32_t row = base + Lay::kOffDS + (t % C::kDsBufs) * Lay::kDSTile + r * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           st_shared_v4(row + ((c ^ (r & 7)) << 4), dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
