@@ -45,7 +45,8 @@ cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
   using C = BwdCfg<D, D == 64 ? 8 : 4>;  // deeper ring at D = 64 (keeps one CTA per SM)
   static std::atomic<bool> attr[64][6] = {};
   const int64_t rows_pad = static_cast<int64_t>(L.params.BH) * L.params.Mpad;
-  const int64_t need = (rows_pad + 7) / 8;
+  const int64_t rows_per_block = 8 * (32 / (D / 8));  // 8 warps, 32 / (D / 8) rows each per pass
+  const int64_t need = (rows_pad + rows_per_block - 1) / rows_per_block;
   const int blocks = static_cast<int>(need < 8LL * sms ? need : 8LL * sms);
   bwd_preprocess_kernel<D><<<blocks, 256, 0, L.stream>>>(
       static_cast<const __nv_bfloat16*>(L.o), static_cast<const __nv_bfloat16*>(L.dout), L.lse, L.nl2, L.dlt,

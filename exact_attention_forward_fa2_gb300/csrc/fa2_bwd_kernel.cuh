@@ -90,7 +90,9 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 // One warp per query row: D_i = sum_d dO[i,d] O[i,d] in fp32 from bf16, and
 // -L_i log2(e), the exponent offset of P = exp2(s scale log2(e) - L_i log2(e)).
 // Rows in [M, Mpad) of every head get D = 0 and -inf.
-// With dQ by reduction it also zeroes the row's D accumulator entries.
+// With dQ by reduction it also zeroes the row's D accumulator entries.  A row
+// is D / 8 lanes with one 16-byte load of O and of dO each (32 / (D / 8) rows
+// per warp per pass).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
                                                              const __nv_bfloat16* __restrict__ dout,
@@ -99,36 +101,40 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
                                                              float* __restrict__ dlt,
                                                              float* __restrict__ dqacc, int M, int Mpad,
                                                              int64_t rows_pad) {
-  constexpr int kPer = D / 32;
+  constexpr int kLanes = D / 8;             // lanes per row
+  constexpr int kRowsPerWarp = 32 / kLanes;
   const int lane = static_cast<int>(threadIdx.x) % 32;
+  const int sub = lane % kLanes;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32; r < rows_pad;
-       r += warps) {
+  for (int64_t r0 = (static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32) * kRowsPerWarp;
+       r0 < rows_pad; r0 += warps * kRowsPerWarp) {
+    const int64_t r = r0 + lane / kLanes;  // rows_pad is a multiple of 128: r < rows_pad
     const int64_t bh = r / Mpad;
     const int i = static_cast<int>(r % Mpad);
     float acc = 0.f;
     if (i < M) {
-      const int64_t off = (bh * M + i) * D + lane * kPer;
+      const int64_t off = (bh * M + i) * D + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + off + e);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(dout + off + e);
-        acc = fmaf(__low2float(a), __low2float(b), acc);
-        acc = fmaf(__high2float(a), __high2float(b), acc);
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&aw[e]);
+        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&bw[e]);
+        acc = fmaf(__low2float(a2), __low2float(b2), acc);
+        acc = fmaf(__high2float(a2), __high2float(b2), acc);
       }
     }
 #pragma unroll
-    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-    if (lane == 0) {
+    for (int sh = kLanes / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (sub == 0) {
       dlt[r] = acc;
       nl2[r] = i < M ? lse[bh * M + i] * -1.4426950408889634f : -INFINITY;
     }
-    if constexpr (kPer % 4 == 0) {
-      if (dqacc) {
-#pragma unroll
-      for (int e = 0; e < kPer; e += 4)
-          *reinterpret_cast<float4*>(dqacc + r * D + lane * kPer + e) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    if (dqacc) {
+      float4* z = reinterpret_cast<float4*>(dqacc + r * D + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
