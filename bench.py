@@ -12,7 +12,9 @@ configuration the >= 50%-of-peak target is stated on); FLOP = 4*B*H*M*N*D / 2.
 
 --pass bwd times the backward (fa2_bwd: dQ, dK, dV from dO, with the forward's O
 and L resident) on the same workload; its FLOP count is the usual 2.5x the
-forward's (five GEMMs of 2*M*N*D per head against the forward's two).
+forward's (five GEMMs of 2*M*N*D per head against the forward's two).  At head
+dim 128 fa2_bwd forms dQ by fp32 reductions (not bitwise reproducible);
+fa2_bwd_deterministic is the two-pass alternative.
 
 --impl reference times the fp64 CPU oracle on the host cores (a bounded sample
 of the same workload per step): the method has no runnable reference
@@ -539,11 +541,13 @@ def run_ours(args, rank, local, world):
         dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
         ws = torch.empty(fa2.lib().fa2_bwd_workspace_bytes(w.B, w.H, w.M), dtype=torch.uint8, device=dev)
         flops = BWD_FLOPS_OVER_FWD * w.flops
-        launches_per_step = 3  # preprocess, dK/dV pass, dQ pass
+        # preprocess, dK/dV pass with dQ by reduction, dQ convert (head dim 128);
+        # preprocess, dK/dV pass, dQ pass (head dim 64)
+        launches_per_step = 3
 
         def step():
             fa2.fa2_bwd(tq, tk, tv, o, lse, tdo, dq=dq, dk=dk, dv=dv, scale=w.scale, causal=w.causal,
-                        workspace=ws, stream=stream)
+                        workspace=ws, stream=stream, deterministic=args.deterministic)
     elif w.modified:
         slopes = torch.from_numpy(si.alibi_slopes(w.H)).to(dev) if w.alibi else None
 
@@ -596,7 +600,7 @@ def run_ours(args, rank, local, world):
         e2e_ins = [(q, tq), (k, tk), (v, tv), (o_host, o), (lse.cpu().numpy(), lse), (do, tdo)]
         e2e_outs = [dq, dk, dv]
     host_step = None
-    if bwd and args.e2e:
+    if bwd and args.e2e and not args.deterministic:  # fa2_bwd_host runs fa2_bwd
         def host_step(hin, hout):
             bf = [t.view(torch.bfloat16) if t.dtype == torch.int16 else t for t in hin + hout]
             fa2.fa2_bwd_host(*bf[:6], dq_host=bf[6], dk_host=bf[7], dv_host=bf[8], scale=w.scale,
@@ -683,7 +687,10 @@ def run_ours(args, rank, local, world):
         "frac_of_peak": roof["frac"],
         "roofline": {**roof,
                      "traffic": dram_traffic_per_launch(w.name, args.pass_),
-                     "kernel": "fa2_bwd (preprocess + dK/dV + dQ kernels)" if bwd else KERNEL,
+                     "kernel": ("fa2_bwd (preprocess + dK/dV/dQ-by-reduction + dQ convert kernels)"
+                                if w.D == 128 and not args.deterministic
+                                else "fa2_bwd%s (preprocess + dK/dV + dQ kernels)"
+                                % ("_deterministic" if args.deterministic else "")) if bwd else KERNEL,
                      "algorithmic_flops_per_launch": flops,
                      "hbm_algorithmic_bytes_per_launch": io,
                      "hbm_gbs_at_this_time": io / (sum(kernel_ms) / len(kernel_ms) / 1e3) / 1e9,
@@ -734,6 +741,8 @@ def main():
                     help="workload to measure (default: the headline bf16 D=128 causal one)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward (default) or the backward pass")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="--pass bwd: time fa2_bwd_deterministic (dQ by a second pass)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")

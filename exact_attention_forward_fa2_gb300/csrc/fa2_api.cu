@@ -291,6 +291,20 @@ int run_forward(const void* q, const void* k, const void* v, void* o, float* lse
   return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
+// Key/value heads per group of the causal dK/dV order.  A group's CTAs run
+// longest first and keep its Q, dO and dQ rows in L2; the groups are few (each
+// at least kBwdGroupWaves full waves of CTAs), so the longest CTAs of the last
+// group still start early enough not to stretch the end of the grid.
+constexpr int64_t kBwdGroupWaves = 4;
+int64_t bwd_head_group(int64_t bh_kv, int64_t n_ktiles) {
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const int64_t groups = std::max<int64_t>(1, bh_kv * n_ktiles / (kBwdGroupWaves * sms));
+  return (bh_kv + groups - 1) / groups;
+}
+
 // Backward workspace: -L log2(e) and D = rowsum(dO o O), [B*H][M rounded up to
 // 128] fp32 each, then the fp32 dQ accumulator of dQ by reduction, [B*H][Mpad][128].
 constexpr int kBwdAccDim = 128;
@@ -535,6 +549,7 @@ int run_backward(const void* q, const void* k, const void* v, const void* o, con
   L.params.nl2 = L.nl2;
   L.params.dlt = L.dlt;
   L.params.dqacc = L.dqacc;
+  L.params.head_group = static_cast<int>(bwd_head_group(bh_kv, n_ktiles));
   L.params.status = st->status;
   L.params.M = M;
   L.params.N = N;

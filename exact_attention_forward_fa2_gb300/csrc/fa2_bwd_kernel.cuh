@@ -57,6 +57,7 @@ struct BwdParams {
   float* dqacc;       // [BH][Mpad][D] fp32 dQ accumulator (dQ by reduction), else null
   int* status;        // sticky device status word
   int M, N, Mpad;     // Mpad = M rounded up to 128
+  int head_group;     // causal dK/dV order: key/value heads per group (BHkv: one group)
   int H, group;       // query heads per batch entry; query heads per key/value head
   int BH, BHkv;       // B * H, B * H_kv
   int n_ktiles;       // ceil(N / 128): key tiles per key/value head
@@ -250,9 +251,15 @@ struct DkvUnit {
 template <bool kCausal>
 __device__ __forceinline__ DkvUnit dkv_unit(const BwdParams& p, int b) {
   DkvUnit u;
-  if (kCausal) {  // smallest key tile first: it has the most query steps
-    u.jt = b / p.BHkv;
-    u.bhkv = b % p.BHkv;
+  if (kCausal) {
+    // groups of head_group key/value heads one after another (their Q, dO and dQ
+    // rows stay in L2); within a group the smallest key tile first, over the
+    // group's heads (it has the most query steps)
+    const int per = p.head_group * p.n_ktiles;
+    const int g = b / per, rem = b - g * per;
+    const int heads = min(p.head_group, p.BHkv - g * p.head_group);
+    u.jt = rem / heads;
+    u.bhkv = g * p.head_group + rem % heads;
   } else {  // tiles of one key/value head adjacent: Q and dO of its heads stay in L2
     u.bhkv = b / p.n_ktiles;
     u.jt = b % p.n_ktiles;
