@@ -2,7 +2,9 @@
 heads overlapped with the compute of other slices.  Each slice is computed by the
 same kernels as a whole-problem call, so the outputs must equal fa2_fwd's (and
 fa2_bwd's) bitwise, for any number of slices, grouped-query heads and page-locked
-or pageable host memory; one forward case is also checked against the oracle."""
+or pageable host memory -- except the backward's dQ at head dim 128, formed by
+fp32 reductions whose order varies from run to run; one forward case is also
+checked against the oracle."""
 import numpy as np
 import pytest
 
@@ -103,8 +105,9 @@ BWD_CASES = [  # (B, H, H_kv, M, N, D, causal)
 @pytest.mark.parametrize("chunks", [0, 1, 3, 99])
 @pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "x".join(map(str, c)))
 def test_host_backward_equals_device_backward(fa2, case, chunks):
-    """fa2_bwd_host: the same kernels per slice of heads, so dq, dk, dv equal
-    fa2_bwd's bitwise for any number of slices."""
+    """fa2_bwd_host: the same kernels per slice of heads, so dk, dv (and dq at
+    head dim 64) equal fa2_bwd's bitwise for any number of slices; dq at head dim
+    128 (by reduction) to within one bf16 ulp of its largest entry."""
     B, H, Hkv, M, N, D, causal = case
     q = si.normal(510, 1, (B, H, M, D), 1.0, si.BF16)
     k = si.normal(510, 2, (B, Hkv, N, D), 1.0, si.BF16)
@@ -118,4 +121,9 @@ def test_host_backward_equals_device_backward(fa2, case, chunks):
     torch.cuda.synchronize()
     dq, dk, dv = fa2.fa2_bwd(hq.cuda(), hk.cuda(), hv.cuda(), o, lse, hdo.cuda(), causal=causal)
     torch.cuda.synchronize()
-    assert torch.equal(dq_h, dq.cpu()) and torch.equal(dk_h, dk.cpu()) and torch.equal(dv_h, dv.cpu())
+    assert torch.equal(dk_h, dk.cpu()) and torch.equal(dv_h, dv.cpu())
+    if D == 64:
+        assert torch.equal(dq_h, dq.cpu())
+    else:
+        ulp = float(dq.float().abs().max()) * 2.0 ** -8
+        assert float((dq_h.float() - dq.cpu().float()).abs().max()) <= ulp
