@@ -56,7 +56,7 @@ cudaError_t launch_all(BwdLaunch& L, int dev, int sms) {
   std::atomic<bool>* a = attr[dev];
   if constexpr (D == 128) {
     if (L.dqacc) {  // dQ by reduction: dK, dV and the dQ accumulator in one pass, then dQ in bf16
-      using CR = BwdCfg<D, 3, true, 2>;  // two dS^T tiles: the P/dS warps never wait for the dQ^T product
+      using CR = BwdCfg<D, 3, true>;  // three stages beside the two dS^T tiles
       e = L.causal ? launch_dkdv<CR, true>(L, a[5]) : launch_dkdv<CR, false>(L, a[4]);
       if (e != cudaSuccess) return e;
       const int64_t n8 = static_cast<int64_t>(L.params.BH) * L.params.M * (D / 8);

@@ -164,12 +164,12 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
 }
 
 // ------------------------------------------------------------------ shared configuration
-template <int D_, int kStages_, bool kDq_ = false, int kDsBufs_ = 1>
+template <int D_, int kStages_, bool kDq_ = false>
 struct BwdCfg {
   static constexpr int D = D_;
   static constexpr int kStages = kStages_;  // depth of the ring of streamed tiles
   static constexpr bool kDq = kDq_;         // dK/dV kernel also forms dQ (by reduction)
-  static constexpr int kDsBufs = kDsBufs_;  // kDq: dS^T tiles in shared memory (1 or 2)
+  static constexpr int kDsBufs = 2;         // kDq: dS^T tiles in shared memory, one per step parity
   static constexpr int BF = 128;            // rows of the fixed tile (keys or queries)
   static constexpr int BS = 64;             // rows of a streamed tile per step
   static constexpr int kColBlocks = D / 64;  // 128-byte column blocks of a bf16 row
@@ -532,15 +532,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
           dk[c4 / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
       }
-      if constexpr (C::kDq && C::kDsBufs == 1) {
-        // the dS^T tile in shared memory is free once the previous step's dQ^T is
-        // complete (with two tiles, the one of step t - 2 is: its dQ^T was issued
-        // before this step's S^T, whose completion the wait on sfull saw)
-        if (t >= 1)
-          ok = __all_sync(0xffffffffu, FA2_BWD_WAIT(bar(Lay::kBarQFull + (t - 1) % 2), ((t - 1) / 2) & 1,
-                                                    kStatusBwdTimeoutSoftmax));
-        if (!ok) break;
-      }
+      // kDq: dS^T tile t % 2 is free: the dQ^T product of step t - 2 that read it
+      // was issued before this step's S^T, whose completion the wait on sfull saw
       tmem_st_x32(tmem + lane_addr + C::kColS(ts), pk);
       tmem_st_x32(tmem + lane_addr + C::kColDS(ts), dk);
       if constexpr (C::kDq) {
