@@ -282,7 +282,9 @@ int fa2_fwd_host(const void* q_host, const void* k_host, const void* v_host, voi
  *   q ... dv        DEVICE buffers of the same shapes (caller-owned); q, k, v, o,
  *                   lse, dout are overwritten by the copies
  *   workspace       as fa2_bwd, sized for the whole problem (every slice reuses it)
- *   chunks          slices (<= 0: 4); at most B*H_kv and 32
+ *   chunks          slices (<= 0: 8 while each slice keeps at least 1.5 waves of
+ *                   the dK/dV kernel's CTAs, B*H_kv*ceil(N/128)/8 >= 1.5 * SMs,
+ *                   else 4); at most B*H_kv and 32
  * Host buffers should be page-locked.  Other arguments and errors as fa2_bwd and
  * fa2_fwd_host; each slice is its own problem with fa2_bwd's kernels, so dk and
  * dv equal fa2_bwd's bitwise and dq (by reduction at D = 128) within its rounding.
