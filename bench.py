@@ -446,6 +446,31 @@ def time_launches(step, flush, stream, warmup: int, reps: int) -> list:
     return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
+def sdpa_same_gpu(w, tq, tk, tv, flush, stream, flops):
+    """PyTorch's scaled_dot_product_attention (the backend torch picks) on the same
+    device tensors and GPU, timed like the forward: the median of 30 launches
+    after 5 warm-ups, the L2 flushed before each.  Context, not a baseline; None
+    for fp32 and score-modified workloads, which it does not express alike."""
+    import torch
+    import torch.nn.functional as F
+    if w.dtype != si.BF16 or w.modified:
+        return None
+    kw = {"is_causal": bool(w.causal), "scale": float(w.scale)}
+    if w.Hkv != w.H:
+        kw["enable_gqa"] = True
+    try:
+        def step():
+            F.scaled_dot_product_attention(tq, tk, tv, **kw)
+        with torch.cuda.stream(stream):
+            ts = sorted(time_launches(step, flush, stream, 5, 30))
+        med = ts[len(ts) // 2]
+        return {"value": flops / (med * 1e-3) / 1e12, "unit": UNIT, "median_ms": med,
+                "torch": torch.__version__, "what": "torch.nn.functional.scaled_dot_product_attention, "
+                "same inputs and GPU, median of 30 launches, L2 flushed before each"}
+    except Exception as e:  # a backend that does not run here is reported, not fatal
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+
+
 def measure_sustained(seconds, flops, step, stream, local, launch_s):
     """Back-to-back launches for about ``seconds`` on the launching stream, with
     no L2 flush between them: the rate a long run settles at under the power cap
@@ -727,6 +752,10 @@ def run_ours(args, rank, local, world):
     else:
         ctx["this_run"] = f"another workload ({w.name}); the pages' shape is bench.py --workload {PAGES_CONTEXT_WORKLOAD}"
     ctx["note"] = "other hardware and precision: context, not a target or a baseline"
+    if args.probes and not bwd:
+        sd = sdpa_same_gpu(w, tq, tk, tv, flush, stream, flops)
+        if sd is not None:
+            ctx["pytorch_sdpa_same_gpu"] = sd
     line["context"] = ctx
     print(json.dumps(line), flush=True)
 
