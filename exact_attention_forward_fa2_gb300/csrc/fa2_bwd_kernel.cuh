@@ -88,8 +88,8 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 }
 
 // ------------------------------------------------------------------ preprocess
-// One warp per query row: D_i = sum_d dO[i,d] O[i,d] in fp32 from bf16, and
-// -L_i log2(e), the exponent offset of P = exp2(s scale log2(e) - L_i log2(e)).
+// Per query row: D_i = sum_d dO[i,d] O[i,d] in fp32 from bf16, and -L_i log2(e),
+// the exponent offset of P = exp2(s scale log2(e) - L_i log2(e)).
 // Rows in [M, Mpad) of every head get D = 0 and -inf.
 // With dQ by reduction it also zeroes the row's D accumulator entries.  A row
 // is D / 8 lanes with one 16-byte load of O and of dO each (32 / (D / 8) rows
@@ -214,7 +214,8 @@ struct DkvLayout {
   static constexpr int kOffRing = kOffV + C::kFixTile;
   // (a stage starts on a 1024-byte boundary, as the 128-byte swizzle requires)
   static constexpr int kStageBytes = (2 * C::kStrTile + 2 * C::BS * 4 + 1023) / 1024 * 1024;
-  // kDq: dS^T of one step, [128 keys][64 queries] bf16 in 128-byte swizzled rows
+  // kDq: dS^T of the last two steps (tile t % 2), each [128 keys][64 queries]
+  // bf16 in 128-byte swizzled rows
   static constexpr int kOffDS = kOffRing + C::kStages * kStageBytes;
   static constexpr int kDSTile = C::BF * 128;
   static constexpr int kDSBytes = C::kDq ? C::kDsBufs * kDSTile : 0;
