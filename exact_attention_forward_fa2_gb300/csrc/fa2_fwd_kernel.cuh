@@ -821,9 +821,15 @@ if constexpr (kWin) {
 }
 
 // ------------------------------------------------------------ set-up
+// Thread 0 also issues the query tiles' loads, before the CTA barrier, so that
+// they overlap the TMEM allocation and the ones fill (measured: +0.7% on the
+// causal 2x16x8192x8192x128 forward, +2% on the TF32 one).  It issues them only
+// when the status word lets the CTA run, so a CTA that skips has no copy in
+// flight when it exits.
 if (threadIdx.x == 0) {
+  const int status = *reinterpret_cast<volatile int*>(p.status);
   misc[1] = 0u;
-  misc[2] = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(p.status));
+  misc[2] = static_cast<uint32_t>(status);
   for (int t = 0; t < C::kQTiles; ++t) {
     mbar_init(bar(C::kBarQ + t), 1);
     mbar_init(bar(C::kBarSFull + t), 1);
@@ -838,6 +844,18 @@ if (threadIdx.x == 0) {
   }
   mbar_init(bar(C::kBarMmaDone), 1);
   fence_mbar_init();
+  if (status == 0) {
+    const uint64_t pol_q = l2_policy_evict_first();
+#pragma unroll
+    for (int t = 0; t < C::kQTiles; ++t) {
+      if (nkv[t] == 0) continue;
+      mbar_arrive_expect_tx(bar(C::kBarQ + t), C::kTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ, bar(C::kBarQ + t),
+                         cb * C::kSwElems, row0[t], tile_head(p, unit, t), pol_q);
+    }
+  }
 }
 if (warp == C::kTmaWarp && lane == 0) {
   prefetch_tensormap(&tmQ);
@@ -870,17 +888,7 @@ if (!skip && warp == C::kTmaWarp) {
   // ---------------------------------------------------------- TMA producer
   if (lane == 0) {
     const uint64_t pol_kv = l2_policy_evict_last();
-    const uint64_t pol_q = l2_policy_evict_first();
-#pragma unroll
-    for (int t = 0; t < C::kQTiles; ++t) {
-      if (nkv[t] == 0) continue;
-      mbar_arrive_expect_tx(bar(C::kBarQ + t), C::kTileBytes);
-#pragma unroll
-      for (int cb = 0; cb < C::kColBlocks; ++cb)
-        tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ,
-                         bar(C::kBarQ + t), cb * C::kSwElems, row0[t], tile_head(p, unit, t), pol_q);
-    }
-    int issued = 0;  // K/V tiles whose loads were issued
+    int issued = 0;  // K/V tiles whose loads were issued (thread 0 issued the query tiles')
     for (int j = 0; j < n_max; ++j) {
       const int s = j % C::kStages;
       const uint32_t use = static_cast<uint32_t>(j / C::kStages);
