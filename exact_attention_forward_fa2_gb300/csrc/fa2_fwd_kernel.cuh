@@ -824,8 +824,13 @@ if constexpr (kWin) {
 // Thread 0 also issues the query tiles' loads, right after the barrier inits
 // and before it reads the status word, so that they overlap that read, the
 // TMEM allocation and the ones fill (measured: +1% on the causal
-// 2x16x8192x8192x128 forward, +3% on the TF32 one).  A CTA that then skips
-// waits for them at the end, before its shared memory is released.
+// 2x16x8192x8192x128 forward, +3% on the TF32 one), and with kEarlyKV the
+// first K/V ring stage's as well, which otherwise waits for the CTA-wide
+// barrier (measured: +1.4% at bf16 D = 64 causal, +1.3% on the sharp
+// 1000 x 3000 cross-attention, +0.7% TF32; -0.3% at bf16 D = 128 causal, which
+// keeps the later issue).  A CTA that then skips waits for them at the end,
+// before its shared memory is released.
+constexpr bool kEarlyKV = !(kCausal && C::D == 128);
 if (threadIdx.x == 0) {
   for (int t = 0; t < C::kQTiles; ++t) {
     mbar_init(bar(C::kBarQ + t), 1);
@@ -851,6 +856,19 @@ if (threadIdx.x == 0) {
       for (int cb = 0; cb < C::kColBlocks; ++cb)
         tma_load_3d_hint(base + C::kOffQ + t * C::kTileBytes + cb * C::kBlockBytes, &tmQ, bar(C::kBarQ + t),
                          cb * C::kSwElems, row0[t], tile_head(p, unit, t), pol_q);
+    }
+    if (kEarlyKV && n_max > 0) {  // stage 0 of the K/V ring
+      const uint64_t pol_kv = l2_policy_evict_last();
+      mbar_arrive_expect_tx(bar(C::kBarKFull), C::kKTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d_hint(base + C::kOffK + cb * C::kKVBlockBytes, &tmK, bar(C::kBarKFull), cb * C::kSwElems,
+                         ks * C::BN, bh_kv, pol_kv);
+      mbar_arrive_expect_tx(bar(C::kBarVFull), C::kKTileBytes);
+#pragma unroll
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d_hint(base + C::kOffV + cb * C::kKVBlockBytes, &tmV, bar(C::kBarVFull), cb * C::kSwElems,
+                         ks * C::BN, bh_kv, pol_kv);
     }
   }
   misc[1] = 0u;
@@ -887,8 +905,10 @@ if (!skip && warp == C::kTmaWarp) {
   // ---------------------------------------------------------- TMA producer
   if (lane == 0) {
     const uint64_t pol_kv = l2_policy_evict_last();
-    int issued = 0;  // K/V tiles whose loads were issued (thread 0 issued the query tiles')
-    for (int j = 0; j < n_max; ++j) {
+    // K/V tiles whose loads were issued (thread 0 issued the query tiles', and
+    // with kEarlyKV stage 0's)
+    int issued = kEarlyKV && n_max > 0 ? 1 : 0;
+    for (int j = issued; j < n_max; ++j) {
       const int s = j % C::kStages;
       const uint32_t use = static_cast<uint32_t>(j / C::kStages);
       // K_j replaces K_{j-S}, free after MMA round j-S; V_j replaces V_{j-S}, free
@@ -1177,10 +1197,14 @@ if (!skip && warp == C::kTmaWarp) {
 }
 
 // ------------------------------------------------------------ teardown
-if (skip && threadIdx.x == 0) {  // the query loads thread 0 issued land before the memory is released
+if (skip && threadIdx.x == 0) {  // the loads thread 0 issued land before the memory is released
 #pragma unroll
   for (int t = 0; t < C::kQTiles; ++t)
     if (nkv[t] > 0) drain_bounded(bar(C::kBarQ + t), 0);
+  if (kEarlyKV && n_max > 0) {
+    drain_bounded(bar(C::kBarKFull), 0);
+    drain_bounded(bar(C::kBarVFull), 0);
+  }
 }
 tc_fence_before_sync();
 __syncthreads();
