@@ -93,6 +93,14 @@ PASS_SOURCES = {
             "fa2_fwd_bf16_d64.cu", "fa2_fwd_bf16_d128.cu", "fa2_fwd_fp32_d64.cu", "fa2_fwd_fp32_d128.cu"),
     "bwd": ("fa2_bwd_kernel.cuh", "fa2_bwd.cu", "fa2_fwd_kernel.cuh", "sm103_ptx.cuh"),
 }
+# workloads measured through the split-KV entry also run the combine kernel
+PASS_SOURCES["splitkv"] = PASS_SOURCES["fwd"] + ("fa2_combine.cu",)
+
+
+def source_key(workload: str, pass_: str) -> str:
+    """Which source list a profile summary of ``workload`` depends on."""
+    w = si.WORKLOADS.get(workload)
+    return "splitkv" if pass_ == "fwd" and w is not None and w.split_kv else pass_
 
 
 def bwd_io_bytes(w) -> int:
@@ -123,7 +131,7 @@ def dram_traffic_per_launch(workload: str = WORKLOAD, pass_: str = "fwd"):
     text = open(path).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(pass_):
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(source_key(workload, pass_)):
         return None
     return float(m_bytes.group(1))
 

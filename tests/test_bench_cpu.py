@@ -39,3 +39,14 @@ def test_traffic_is_dropped_once_the_sources_change(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda pass_="fwd": "0" * 16)
     assert bench.dram_traffic_per_launch(HEADLINE.name, "fwd") is None
     assert bench.dram_traffic_per_launch(HEADLINE.name, "bwd") is None
+
+
+def test_split_kv_profiles_depend_on_the_combine_source():
+    """Workloads measured through the split-KV entry also run the combine kernel,
+    so their profile summaries are keyed to a source list that includes it."""
+    assert bench.source_key("bf16_1x32x128x32768x128_gqa8_splitkv", "fwd") == "splitkv"
+    assert bench.source_key("bf16_16x32x1x8192x128_gqa8_decode", "fwd") == "splitkv"
+    assert bench.source_key(HEADLINE.name, "fwd") == "fwd"
+    assert bench.source_key(HEADLINE.name, "bwd") == "bwd"
+    assert set(bench.PASS_SOURCES["fwd"]) < set(bench.PASS_SOURCES["splitkv"])
+    assert "fa2_combine.cu" in bench.PASS_SOURCES["splitkv"]
